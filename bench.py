@@ -1,0 +1,436 @@
+"""Benchmark: paged decode-attention KV GB/s and tokens/s on GB300.
+
+A step is one pass of the whole hot path over one batch:
+  copy_blocks (if the step has copy-on-write pairs) -> slot mapping ->
+  reshape_and_cache of the new tokens -> paged decode attention (+ merge).
+Default workload: the LLaMA-7B-shaped layer -- 64 sequences, 32 heads x 128,
+fp16, block size 16, context ~ U{128..2048}, pool = need + 10 %, shuffled
+placement, one new token per sequence.
+
+value  = logical KV bytes read per step (sum ctx * H * D * 2 * 2 B) / step time
+e2e    = the same metric with each step's inputs copied from pinned host
+         memory and its output copied back inside the timed region
+--impl reference times the fp64 CPU oracle on the host cores instead.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun every rank runs its own batch (weak scaling, no collective on
+the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode-attn KV GB/s (% of GB300 HBM peak) and tokens/s at 1 GPU"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+DECODE_SOURCES = ["paged_kv_cache_162_gb300/csrc/decode.cu",
+                  "paged_kv_cache_162_gb300/csrc/pkv_device.cuh"]
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="llama7b_batch64")
+    p.add_argument("--partition-tokens", type=int, default=0)
+    p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------------ helpers
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest(paths=DECODE_SOURCES) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if the
+    decode sources are unchanged since that capture; else None."""
+    path = os.path.join(ROOT, "profiles", f"decode_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    d = re.search(r"decode_source_digest:\s*([0-9a-f]+)", text)
+    if not m or not d or d.group(1) != source_digest():
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        rows = []
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        sms = sorted(r[0] for r in rows)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2]) if v == "Active"})
+        return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------- workloads
+def describe(w):
+    ctx = w.context_lens
+    return {"workload": w.name, "seqs": w.S, "heads": w.H, "head_dim": w.D, "block_size": w.bs,
+            "pool_blocks": w.NB, "context_min": int(ctx.min()), "context_max": int(ctx.max()),
+            "context_sum": int(ctx.sum()), "new_tokens": w.T,
+            "kv_bytes_per_step": w.kv_bytes()}
+
+
+def make_workload(name, rank):
+    import workloads as W
+    seed_shift = 7919 * rank  # each rank its own batch
+    if name == "llama7b_batch64":
+        return W.llama7b_batch64(seed=1001 + seed_shift)
+    if name == "continuous_batching_bf16":
+        return W.continuous_batching_bf16(seed=1002 + seed_shift)
+    if name == "shared_prefix":
+        return W.shared_prefix(seed=1003 + seed_shift)
+    if name == "shared_prefix_cow":
+        return W.shared_prefix(seed=1003 + seed_shift, cow=True)
+    if name.startswith("long_context_bs"):
+        return W.long_context(bs=int(name[len("long_context_bs"):]), seed=1004 + seed_shift)
+    if name == "tiny":
+        return W.tiny(seed=1000 + seed_shift)
+    raise SystemExit(f"unknown workload {name}")
+
+
+# --------------------------------------------------------- oracle timing
+def time_oracle(w, seconds_per_step=2.0):
+    """Times one oracle step (slot mapping, cache write, fp64 decode) over a
+    bounded sample of the workload: the first n (sequence, head) pairs in
+    sequence order, n calibrated so that the step takes about
+    `seconds_per_step`.  Returns (seconds, sample_bytes, sample_seqs,
+    threads, fn) where fn() re-runs the same sample."""
+    import numpy as np
+    from oracle import kernels as K
+    from oracle import step as OS
+    import workloads as W
+
+    threads = K.default_threads()
+    a, tables, nb, pairs = OS.plan(w)
+    ids, rob, k_pool, v_pool = OS.build_pool(w, tables, pairs, W.POISON[w.dtype])
+    ctx = w.context_lens.astype(np.int64)
+    per_tok = w.D * 2 * 2  # K and V bytes of one token of one head
+    all_items = np.array([[s, h] for s in range(w.S) for h in range(w.H)], dtype=np.int32)
+    item_bytes = ctx[all_items[:, 0]] * per_tok
+
+    def run_items(items, tok):
+        K.copy_blocks(k_pool, v_pool, pairs, row_of_block=rob)
+        slots = K.slot_mapping(tables, w.seq_idx[tok], w.pos[tok], w.bs)
+        K.reshape_and_cache(k_pool, v_pool, w.new_k[tok], w.new_v[tok], slots, row_of_block=rob)
+        K.decode(w.q, k_pool, v_pool, tables, w.context_lens, w.scale, w.dtype == W.BF16,
+                 row_of_block=rob, items=items, nthreads=threads)
+
+    # calibrate on about 1 % of the workload (at least one item per thread)
+    n_cal = int(min(len(all_items), max(threads, len(all_items) // 100)))
+    t0 = time.perf_counter()
+    run_items(all_items[:n_cal], np.zeros(len(w.seq_idx), dtype=bool))
+    rate = item_bytes[:n_cal].sum() / max(time.perf_counter() - t0, 1e-6)
+    cum = np.cumsum(item_bytes)
+    n = int(np.searchsorted(cum, rate * seconds_per_step)) + 1
+    n = max(1, min(n, len(all_items)))
+    items = all_items[:n]
+    seqs = np.unique(items[:, 0])
+    tok = np.isin(w.seq_idx, seqs)
+    sample_bytes = int(item_bytes[:n].sum())
+
+    def one():
+        run_items(items, tok)
+
+    t0 = time.perf_counter()
+    one()
+    dt = time.perf_counter() - t0
+    return dt, sample_bytes, n / w.H, threads, one
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = make_workload(args.workload, 0)
+    # each step a bounded sample, so that warmup + steps take ~2.5 minutes
+    per_step = min(2.0, max(0.02, 150.0 / (args.steps + args.warmup + 1)))
+    dt, sample_bytes, nseq, threads, one = time_oracle(w, per_step)
+    for _ in range(max(0, args.warmup)):
+        one()
+    times = []
+    for _ in range(max(1, args.steps)):
+        t0 = time.perf_counter()
+        one()
+        times.append(time.perf_counter() - t0)
+    t = sum(times) / len(times)
+    gbs = sample_bytes / t / 1e9
+    tok_s = nseq / t
+    sample = (f"first {int(round(nseq * w.H))} (sequence, head) pairs of {w.name} in sequence "
+              f"order ({nseq:.2f} of {w.S} sequences), {sample_bytes / 1e6:.1f} MB of logical "
+              f"KV per step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world,
+        "steps": len(times), "warmup": args.warmup, "ms_per_step": t * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": describe(w), "tokens_per_s": tok_s,
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------- our path
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import workloads as W
+    from paged_kv_cache_162_gb300 import _lib as L
+    from paged_kv_cache_162_gb300.engine import DecodeStep, dtype_code
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    w = make_workload(args.workload, rank)
+    st = DecodeStep(dtype=w.dtype, S=w.S, H=w.H, D=w.D, bs=w.bs, NB=w.NB, MB=w.MB, scale=w.scale,
+                    ctx_before=w.ctx_before, n_new=w.n_new, tables_pre=w.tables_pre,
+                    nblocks_pre=w.nblocks_pre, initial_free=w.initial_free, blocks=w.blocks,
+                    k_blocks=w.k_blocks, v_blocks=w.v_blocks, q=w.q, new_k=w.new_k,
+                    new_v=w.new_v, seq_idx=w.seq_idx, pos=w.pos,
+                    fill_bits=int(W.POISON[w.dtype]), partition_tokens=args.partition_tokens,
+                    device=dev)
+    st.plan()
+    stream = torch.cuda.Stream(device=dev)
+    kv_bytes = w.kv_bytes()
+    # algorithmic bytes of one decode launch: KV rows + q + out + table entries
+    dec_bytes = (kv_bytes + 2 * w.S * w.H * w.D * 2
+                 + int(np.ceil(w.context_lens / w.bs).sum()) * 4)
+    launches_per_step = (1 if len(st.pairs_host) else 0) + (2 if w.T else 0) + 2
+
+    ev = {}
+
+    def step(record=None):
+        if len(st.pairs_host):
+            from paged_kv_cache_162_gb300.engine import copy_blocks
+            copy_blocks(st.k_cache, st.v_cache, st.pairs, stream)
+        if w.T:
+            from paged_kv_cache_162_gb300.engine import compute_slot_mapping, reshape_and_cache
+            compute_slot_mapping(st.slot_mapping, st.block_tables, st.seq_idx, st.pos, w.bs,
+                                 stream)
+            reshape_and_cache(st.new_k, st.new_v, st.k_cache, st.v_cache, st.slot_mapping, stream)
+        if record is not None:
+            record[0].record(stream)
+        st.decode(stream)
+        if record is not None:
+            record[1].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+    stream.synchronize()
+    L.pkv_sync_check(stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # ---- device-resident timed region
+    K = max(1, args.steps)
+    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        time.sleep(0.05)
+        with torch.cuda.stream(stream):
+            t_start.record(stream)
+            for i in range(K):
+                step(dec_ev[i])
+            t_end.record(stream)
+        stream.synchronize()
+    torch.cuda.synchronize()
+    barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    dec_ms = sum(a.elapsed_time(b) for a, b in dec_ev) / K
+    L.pkv_sync_check(stream)
+    errs = L.pkv_get_device_errors()
+    if errs:
+        raise SystemExit(f"device error word set: {errs:#x}")
+
+    # ---- end to end: host buffers, copies inside the timed region
+    pin = lambda t: t.cpu().pin_memory()
+    host_in = {"q": pin(st.q), "new_k": pin(st.new_k), "new_v": pin(st.new_v),
+               "block_tables": pin(st.block_tables), "context_lens": pin(st.context_lens),
+               "seq_idx": pin(st.seq_idx), "pos": pin(st.pos)}
+    if len(st.pairs_host):
+        host_in["pairs"] = pin(st.pairs)
+    host_out = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+    dev_in = {"q": st.q, "new_k": st.new_k, "new_v": st.new_v, "block_tables": st.block_tables,
+              "context_lens": st.context_lens, "seq_idx": st.seq_idx, "pos": st.pos}
+    if len(st.pairs_host):
+        dev_in["pairs"] = st.pairs
+
+    def e2e_step():
+        for k, t in host_in.items():
+            dev_in[k].copy_(t, non_blocking=True)
+        step()
+        host_out.copy_(st.out, non_blocking=True)
+        stream.synchronize()
+
+    E = max(1, args.e2e_steps)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+        barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(E):
+            e2e_step()
+        e1.record(stream)
+        stream.synchronize()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / E
+
+    # ---- max over ranks
+    step_ms = total_ms / K
+    if world > 1:
+        t = torch.tensor([step_ms, e2e_ms, dec_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms, e2e_ms, dec_ms = t.tolist()
+    peak, peak_kind = measured_peak()
+    value = world * kv_bytes / (step_ms * 1e-3) / 1e9
+    achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
+    traffic = profiled_traffic(args.workload)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        dt, sample_bytes, nseq, threads, _ = time_oracle(w)
+        cpu = {"value": sample_bytes / dt / 1e9, "unit": "GB/s", "cores": threads,
+               "kind": "oracle",
+               "sample": f"one oracle step (slot mapping, cache write, fp64 decode) over the "
+                         f"first {int(round(nseq * w.H))} (sequence, head) pairs in sequence "
+                         f"order ({nseq:.2f} of {w.S} sequences, "
+                         f"{sample_bytes / 1e6:.1f} MB logical KV), {dt:.2f} s"}
+
+    if rank == 0:
+        cfg = describe(w)
+        cfg.update({"partition_tokens": args.partition_tokens or 256,
+                    "l2": f"inputs larger than L2: {kv_bytes / 1e9:.2f} GB of KV read per step "
+                          f"vs 129 MB L2; no flush",
+                    "parallelism": f"replicas{world}" if world > 1 else "single GPU",
+                    "global_batch": w.S * world})
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": step_ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": cfg,
+            "tokens_per_s": world * w.S / (step_ms * 1e-3),
+            "pct_of_hbm_peak": {"of_measured": value / peak, "of_nominal_8000": value / NOMINAL_HBM_GBS},
+            "decode_ms": dec_ms,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": peak_kind, "kernel": "pkv paged_attention_decode (plan + decode)",
+                         "algorithmic_bytes_per_launch": dec_bytes},
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * kv_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": launches_per_step * K,
+            "clocks": clocks.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

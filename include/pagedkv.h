@@ -1,0 +1,234 @@
+/*
+ * pagedkv -- paged KV-cache decode attention for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI of the library libpagedkv.so.  Every entry point is `extern "C"`,
+ * takes plain pointers and sizes, and returns a pkv_status.  No exception
+ * crosses this boundary.
+ *
+ * Sources (web pages on PagedAttention; cited by title and section):
+ *  [P1] "3.3 页面级显存管理" (page-level GPU memory management)
+ *  [P2] "vLLM三大核心技术分页内存与共享解码" (vLLM core techniques)
+ *  [P3] "3.1 PagedAttention的核心原理" (PagedAttention core principles)
+ *  [P4] notes on "vLLM: Easy, Fast, and Cheap LLM Serving with PagedAttention"
+ *
+ * Conventions shared by every device entry point
+ *  - Device pointers are caller-owned device memory; the library allocates
+ *    no device memory.  Token data (q, K, V, out, key, value) is 16-bit
+ *    (pkv_dtype) and every such pointer must be 16-byte aligned.
+ *  - KV cache layout ([P3] 3.1.2 "页面结构设计", 3.1.3 step 4): separate K
+ *    and V caches, each [NB][bs][H][D] row-major.  Token offset o of
+ *    physical block p, head h, dim d sits at ((p*bs + o)*H + h)*D + d, i.e.
+ *    physical_page*page_size*kv_dim + page_offset*kv_dim with kv_dim = H*D.
+ *  - Block tables ([P2] "KV Cache逻辑块物理块映射机制", [P3] 3.1.3, [P4]
+ *    "关键误解"): one flat int32 row of MB entries per sequence, row-major
+ *    [S][MB]; entry j is the physical block of logical block j.  Only the
+ *    first ceil(context_len/bs) entries of a row are read.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Kernels run asynchronously on it; a launch error is returned
+ *    at once, an error raised while a kernel runs surfaces on a later call
+ *    or through pkv_sync_check().
+ *  - Supported shapes: D (head_dim) in {64, 128}, bs (block size) in
+ *    {16, 32}; anything else returns PKV_ERR_UNSUPPORTED.
+ *  - Out-of-range ids (a physical block outside [0, NB), a slot outside
+ *    [0, NB*bs), a context longer than MB*bs) are never dereferenced: the
+ *    kernel skips the access and records PKV_DEVERR_* in a device error word
+ *    that pkv_get_device_errors() returns.
+ *  - pkv_last_error_string() describes the last failure of this thread.
+ *
+ * The host block allocator (pkv_alloc_*) is not thread-safe: the caller
+ * serialises calls on one handle, as the pages' single scheduler does.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size or id   */
+    PKV_ERR_UNSUPPORTED = 2, /* head_dim / block_size / dtype not built   */
+    PKV_ERR_OOM = 3,         /* allocator: not enough free blocks          */
+    PKV_ERR_WORKSPACE = 4,   /* decode: workspace too small               */
+    PKV_ERR_CUDA = 5         /* a CUDA runtime call failed                */
+} pkv_status;
+
+typedef enum { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+/* Bits of the device error word (pkv_get_device_errors). */
+#define PKV_DEVERR_BLOCK_ID 0x1  /* block table entry outside [0, NB)     */
+#define PKV_DEVERR_SLOT 0x2      /* slot outside [0, NB*bs) (and >= 0)    */
+#define PKV_DEVERR_CONTEXT 0x4   /* context_len < 0 or > max context      */
+#define PKV_DEVERR_POSITION 0x8  /* slot mapping: position past the table */
+
+/* Thread-local text of the last error ("" if none).  Never NULL. */
+const char* pkv_last_error_string(void);
+
+/* Library version string. */
+const char* pkv_version(void);
+
+/* ------------------------------------------------------------------ *
+ * Decode attention
+ * ------------------------------------------------------------------ */
+
+/* Bytes of device workspace pkv_paged_attention_decode needs for S
+ * sequences, H heads, head_dim D, contexts of at most max_context_len tokens
+ * and partitions of partition_tokens tokens (0 = library default).  The
+ * workspace holds the work list, per-partition softmax partials (running
+ * max, running sum and the unnormalised output, fp32) and merge tickets.
+ * Returns 0 for invalid arguments. */
+size_t pkv_decode_workspace_size(int S, int H, int D, int max_context_len,
+                                 int partition_tokens);
+
+/* Single-query decode attention over the paged cache.
+ *
+ * For every sequence s and head h, with n = context_lens[s]:
+ *   out[s,h,:] = sum_{j<n} softmax_j(scale * q[s,h,:] . K_j) V_j
+ * where K_j, V_j are the cache rows of token j, found by address
+ * translation: logical = j / bs, offset = j % bs, physical =
+ * block_tables[s*MB + logical] ([P3] 3.1.3 steps 1-4; [P4] "疑问" 1).
+ * n = 0 gives out = 0.  num_kv_heads = num_heads (multi-head attention).
+ *
+ *   out           [S][H][D] dtype, written
+ *   q             [S][H][D] dtype
+ *   k_cache, v_cache  [NB][bs][H][D] dtype, read only
+ *   block_tables  [S][MB] int32
+ *   context_lens  [S] int32, each in [0, max_context_len]
+ *   max_context_len  upper bound of context_lens (0 = MB*bs); at most MB*bs
+ *   scale         logit scale (usually 1/sqrt(D))
+ *   partition_tokens  tokens per split-K partition, a multiple of 16 and of
+ *                 bs (0 = library default).  Contexts longer than one
+ *                 partition are split; each partition's (max, sum, output)
+ *                 is merged by the last partition to finish.
+ *   workspace     device memory of at least pkv_decode_workspace_size(S, H,
+ *                 D, max_context_len, partition_tokens) bytes, 256-byte
+ *                 aligned; no initial contents needed.  One call at a time
+ *                 may use a workspace (calls that overlap on the GPU race).
+ * Computation is fp32 with one round-to-nearest-even to dtype at the end.
+ */
+pkv_status pkv_paged_attention_decode(
+    void* out, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, const int32_t* context_lens,
+    int S, int H, int D, int bs, int NB, int MB, int max_context_len,
+    float scale, pkv_dtype dtype, int partition_tokens,
+    void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------ *
+ * Cache maintenance kernels
+ * ------------------------------------------------------------------ */
+
+/* Slot of each new token (address translation, [P3] 3.1.3 steps 1-3):
+ *   slot_mapping[t] = block_tables[seq_idx[t]*MB + pos[t]/bs]*bs + pos[t]%bs
+ * pos[t] < 0 gives -1 (no write).  A position past the row (pos/bs >= MB)
+ * or a seq_idx outside [0, S) gives -1 and sets PKV_DEVERR_POSITION.
+ *   slot_mapping  [T] int64 device, written
+ *   block_tables  [S][MB] int32 device; seq_idx, pos: [T] int32 device   */
+pkv_status pkv_compute_slot_mapping(int64_t* slot_mapping, const int32_t* block_tables,
+                                    const int32_t* seq_idx, const int32_t* pos,
+                                    int T, int S, int MB, int bs, void* stream);
+
+/* Write new tokens' K and V into their slots (the "write the new KV data
+ * into the block" step of [P2] "Copy-on-Write共享解码的显存优化原理"):
+ *   k_cache[slot/bs][slot%bs][h][:] = key[t][h][:], same for V,
+ * for every t with slot_mapping[t] >= 0 (negative = skip).  Slots must be
+ * distinct within a call.
+ *   key, value  [T][H][D] dtype device;  slot_mapping [T] int64 device   */
+pkv_status pkv_reshape_and_cache(const void* key, const void* value, void* k_cache,
+                                 void* v_cache, const int64_t* slot_mapping, int T,
+                                 int H, int D, int bs, int NB, pkv_dtype dtype,
+                                 void* stream);
+
+/* Copy-on-write block copies ([P2] "Copy-on-Write共享解码的显存优化原理";
+ * [P3] 3.1.5 step 3): for each of the P pairs (src, dst) in block_mapping
+ * ([P][2] int64 device), copy all bs*H*D elements of K block src to K block
+ * dst and likewise for V.  No dst may appear twice or also be a src in the
+ * same call (the allocator's copies always target fresh blocks).  P = 0 is
+ * a no-op. */
+pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapping,
+                           int P, int H, int D, int bs, int NB, pkv_dtype dtype,
+                           void* stream);
+
+/* Waits for `stream`, then returns PKV_ERR_CUDA if any asynchronous CUDA
+ * error is pending. */
+pkv_status pkv_sync_check(void* stream);
+
+/* Reads and clears the device error word (PKV_DEVERR_* bits) of the
+ * current device.  Synchronises with the device. */
+pkv_status pkv_get_device_errors(int32_t* flags);
+
+/* ------------------------------------------------------------------ *
+ * Host block allocator: one global pool of physical blocks with a free
+ * list and a reference count per physical block ([P1] 3.3.2 and 3.3.4;
+ * [P2] "Copy-on-Write共享解码的显存优化原理"; [P3] 3.1.2, 3.1.5; [P4]
+ * "Memory Sharing与写时复制": the count lives with the physical block).
+ * The free list is a stack: the block freed last is handed out first; a
+ * fresh pool hands out NB-1 first.  Every operation is all-or-nothing.
+ * ------------------------------------------------------------------ */
+typedef struct pkv_allocator pkv_allocator;
+
+/* A pool of num_blocks free blocks. */
+pkv_status pkv_alloc_create(int32_t num_blocks, pkv_allocator** out);
+
+/* A pool whose free list is initial_free[0..n_free) (the last element is
+ * handed out first); every block of [0, num_blocks) not listed is held once
+ * (refcount 1).  Ids must be distinct and in range. */
+pkv_status pkv_alloc_create_with_order(int32_t num_blocks, const int32_t* initial_free,
+                                       int32_t n_free, pkv_allocator** out);
+
+void pkv_alloc_destroy(pkv_allocator* a);
+
+/* Take n blocks (refcount 1 each) into out_ids[0..n).  PKV_ERR_OOM takes
+ * nothing ([P1] 3.3.2 allocator sketch checks before taking). */
+pkv_status pkv_alloc_blocks(pkv_allocator* a, int32_t n, int32_t* out_ids);
+
+/* One more holder for each block (sharing a prefix / forking a sequence,
+ * [P1] 3.3.2 share_blocks; [P3] 3.1.5 step 2).  Every id must be held. */
+pkv_status pkv_alloc_incref(pkv_allocator* a, const int32_t* ids, int32_t n);
+
+/* One holder fewer for each block; a block whose count reaches 0 returns to
+ * the free list ([P2] "引用计数机制还服务于Block的回收").  Releasing a block
+ * that is not held is PKV_ERR_INVALID_ARG (nothing changes).
+ * *num_freed (may be NULL) receives the number of blocks freed. */
+pkv_status pkv_alloc_decref(pkv_allocator* a, const int32_t* ids, int32_t n,
+                            int32_t* num_freed);
+
+/* Copy-on-write before a write into block id: at refcount 1 *out_id = id
+ * and *needs_copy = 0; otherwise a new block is taken (PKV_ERR_OOM leaves
+ * everything unchanged), id loses one holder, *out_id = the new block and
+ * *needs_copy = 1: the caller copies id -> *out_id (pkv_copy_blocks) and
+ * points its table at *out_id ([P2] "Copy-on-Write共享解码的显存优化原理";
+ * [P3] 3.1.5 steps 3-4). */
+pkv_status pkv_alloc_cow(pkv_allocator* a, int32_t id, int32_t* out_id, int32_t* needs_copy);
+
+/* Make room for tokens [ctx_before, ctx_before + n_new) of one sequence
+ * whose block table row is table[0..*num_blocks) (capacity max_blocks):
+ * first every existing block those tokens land in that has refcount > 1 is
+ * copied-on-write (in logical order; its (src, dst) pair is appended to
+ * pairs[2*k], pairs[2*k+1] and the table entry repointed); then as many
+ * new blocks are appended as ceil((ctx_before + n_new)/bs) requires ([P1]
+ * 3.3.2: batch allocation at prefill, one more block whenever the token
+ * count exceeds num_blocks*bs).  *n_pairs receives the number of pairs;
+ * `pairs` needs room for 2*ceil(n_new/bs + 1) int64.  All-or-nothing:
+ * PKV_ERR_OOM or PKV_ERR_INVALID_ARG leave table, counts and pool as they
+ * were. */
+pkv_status pkv_alloc_append(pkv_allocator* a, int32_t* table, int32_t* num_blocks,
+                            int32_t max_blocks, int32_t ctx_before, int32_t n_new,
+                            int32_t bs, int64_t* pairs, int32_t* n_pairs);
+
+/* Reference count of block id (0 = free). */
+pkv_status pkv_alloc_refcount(const pkv_allocator* a, int32_t id, int32_t* rc);
+
+int32_t pkv_alloc_num_blocks(const pkv_allocator* a);
+int32_t pkv_alloc_num_free(const pkv_allocator* a);
+/* Blocks held more than once (refcount > 1). */
+int32_t pkv_alloc_num_shared(const pkv_allocator* a);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

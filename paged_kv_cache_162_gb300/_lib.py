@@ -1,0 +1,174 @@
+"""ctypes binding of libpagedkv.so: the C ABI of include/pagedkv.h under the
+same names.  Argument marshalling only -- every computation runs in the
+library.  A pointer argument may be an int address, a torch.Tensor
+(data_ptr()) or a numpy array (host memory); `stream` may be None (the
+current torch CUDA stream), an int handle or a torch.cuda.Stream.
+
+Loading fails loudly if the library has not been built: there is no
+fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libpagedkv.so")
+
+PKV_OK = 0
+PKV_ERR_INVALID_ARG = 1
+PKV_ERR_UNSUPPORTED = 2
+PKV_ERR_OOM = 3
+PKV_ERR_WORKSPACE = 4
+PKV_ERR_CUDA = 5
+PKV_F16 = 0
+PKV_BF16 = 1
+PKV_DEVERR_BLOCK_ID = 0x1
+PKV_DEVERR_SLOT = 0x2
+PKV_DEVERR_CONTEXT = 0x4
+PKV_DEVERR_POSITION = 0x8
+
+_STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
+                 3: "PKV_ERR_OOM", 4: "PKV_ERR_WORKSPACE", 5: "PKV_ERR_CUDA"}
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class OutOfBlocks(PkvError, MemoryError):
+    pass
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I32 = ctypes.c_int32
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+
+# name -> (restype, argtypes); the order follows include/pagedkv.h
+SIGNATURES = {
+    "pkv_last_error_string": (ctypes.c_char_p, []),
+    "pkv_version": (ctypes.c_char_p, []),
+    "pkv_decode_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "pkv_paged_attention_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
+                                        _I, _P, _SZ, _P]),
+    "pkv_compute_slot_mapping": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P]),
+    "pkv_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "pkv_copy_blocks": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "pkv_sync_check": (_I, [_P]),
+    "pkv_get_device_errors": (_I, [_P]),
+    "pkv_alloc_create": (_I, [_I32, _P]),
+    "pkv_alloc_create_with_order": (_I, [_I32, _P, _I32, _P]),
+    "pkv_alloc_destroy": (None, [_P]),
+    "pkv_alloc_blocks": (_I, [_P, _I32, _P]),
+    "pkv_alloc_incref": (_I, [_P, _P, _I32]),
+    "pkv_alloc_decref": (_I, [_P, _P, _I32, _P]),
+    "pkv_alloc_cow": (_I, [_P, _I32, _P, _P]),
+    "pkv_alloc_append": (_I, [_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P]),
+    "pkv_alloc_refcount": (_I, [_P, _I32, _P]),
+    "pkv_alloc_num_blocks": (_I32, [_P]),
+    "pkv_alloc_num_free": (_I32, [_P]),
+    "pkv_alloc_num_shared": (_I32, [_P]),
+}
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(
+                f"{LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; "
+                f"g.build()\"` (no fallback implementation exists)")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def ptr(x) -> int | None:
+    """Address of a tensor / numpy array / int (None stays None)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if hasattr(x, "ctypes"):
+        return x.ctypes.data
+    raise TypeError(f"cannot take the address of {type(x)}")
+
+
+def stream_handle(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def check(status: int, what: str = "") -> None:
+    if status != PKV_OK:
+        msg = lib().pkv_last_error_string().decode(errors="replace")
+        exc = OutOfBlocks if status == PKV_ERR_OOM else PkvError
+        raise exc(status, msg or what)
+
+
+# ---------------------------------------------------------------- entries
+def pkv_last_error_string() -> str:
+    return lib().pkv_last_error_string().decode(errors="replace")
+
+
+def pkv_version() -> str:
+    return lib().pkv_version().decode()
+
+
+def pkv_decode_workspace_size(S, H, D, max_context_len, partition_tokens=0) -> int:
+    return int(lib().pkv_decode_workspace_size(S, H, D, max_context_len, partition_tokens))
+
+
+def pkv_paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, S, H, D, bs,
+                               NB, MB, max_context_len, scale, dtype, partition_tokens, workspace,
+                               workspace_bytes, stream=None) -> None:
+    check(lib().pkv_paged_attention_decode(
+        ptr(out), ptr(q), ptr(k_cache), ptr(v_cache), ptr(block_tables), ptr(context_lens), S, H,
+        D, bs, NB, MB, max_context_len, float(scale), int(dtype), partition_tokens, ptr(workspace),
+        int(workspace_bytes), stream_handle(stream)), "paged_attention_decode")
+
+
+def pkv_compute_slot_mapping(slot_mapping, block_tables, seq_idx, pos, T, S, MB, bs,
+                             stream=None) -> None:
+    check(lib().pkv_compute_slot_mapping(ptr(slot_mapping), ptr(block_tables), ptr(seq_idx),
+                                         ptr(pos), T, S, MB, bs, stream_handle(stream)),
+          "compute_slot_mapping")
+
+
+def pkv_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, T, H, D, bs, NB, dtype,
+                          stream=None) -> None:
+    check(lib().pkv_reshape_and_cache(ptr(key), ptr(value), ptr(k_cache), ptr(v_cache),
+                                      ptr(slot_mapping), T, H, D, bs, NB, int(dtype),
+                                      stream_handle(stream)), "reshape_and_cache")
+
+
+def pkv_copy_blocks(k_cache, v_cache, block_mapping, P, H, D, bs, NB, dtype, stream=None) -> None:
+    check(lib().pkv_copy_blocks(ptr(k_cache), ptr(v_cache), ptr(block_mapping), P, H, D, bs, NB,
+                                int(dtype), stream_handle(stream)), "copy_blocks")
+
+
+def pkv_sync_check(stream=None) -> None:
+    check(lib().pkv_sync_check(stream_handle(stream)), "sync_check")
+
+
+def pkv_get_device_errors() -> int:
+    v = ctypes.c_int32(0)
+    check(lib().pkv_get_device_errors(ctypes.addressof(v)), "get_device_errors")
+    return int(v.value)

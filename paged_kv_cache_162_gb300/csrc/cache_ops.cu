@@ -1,0 +1,158 @@
+// Cache maintenance kernels: slot mapping, the KV write of new tokens
+// (reshape_and_cache) and the copy-on-write block copy (copy_blocks).
+//
+// All three move 16-byte vectors.  In the [NB][bs][H][D] layout a token's K
+// (or V) for all heads is one contiguous row of H*D elements and a block is
+// one contiguous run of bs*H*D elements, so both copies are plain streams of
+// 16-byte loads and stores.
+#include "pagedkv.h"
+#include "pkv_device.cuh"
+
+namespace {
+
+// Address translation of "3.1 PagedAttention的核心原理" 3.1.3 steps 1-3:
+// logical block = pos / bs, offset = pos % bs, physical = table[logical];
+// the slot is the token's row physical*bs + offset.
+__global__ void slot_mapping_kernel(int64_t* __restrict__ slot, const int32_t* __restrict__ bt,
+                                    const int32_t* __restrict__ seq_idx,
+                                    const int32_t* __restrict__ pos, int T, int S, int MB, int bs,
+                                    int* err) {
+    int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= T) return;
+    int p = pos[t];
+    int s = seq_idx[t];
+    if (p < 0) {
+        slot[t] = -1;
+        return;
+    }
+    int logical = p / bs;
+    if (logical >= MB || s < 0 || s >= S) {
+        pkv::report(err, PKV_DEVERR_POSITION);
+        slot[t] = -1;
+        return;
+    }
+    int64_t phys = bt[(int64_t)s * MB + logical];
+    slot[t] = phys * bs + (p - logical * bs);
+}
+
+// One CTA per new token: copy its H*D-element K row and V row into the
+// slot's row of each cache.
+__global__ void __launch_bounds__(256) reshape_and_cache_kernel(
+    const uint4* __restrict__ key, const uint4* __restrict__ value, uint4* __restrict__ k_cache,
+    uint4* __restrict__ v_cache, const int64_t* __restrict__ slot_mapping, int vec_per_row,
+    int64_t num_slots, int* err) {
+    const int t = blockIdx.x;
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) return;
+    if (slot >= num_slots) {
+        if (threadIdx.x == 0) pkv::report(err, PKV_DEVERR_SLOT);
+        return;
+    }
+    const uint4* ks = key + (int64_t)t * vec_per_row;
+    const uint4* vs = value + (int64_t)t * vec_per_row;
+    uint4* kd = k_cache + slot * vec_per_row;
+    uint4* vd = v_cache + slot * vec_per_row;
+    for (int i = threadIdx.x; i < vec_per_row; i += blockDim.x) {
+        uint4 a = ks[i];
+        uint4 b = vs[i];
+        kd[i] = a;
+        vd[i] = b;
+    }
+}
+
+// Grid (P, splits): CTA (p, y) copies the y-th 1/splits of pair p's K block
+// and V block.
+__global__ void __launch_bounds__(256) copy_blocks_kernel(
+    uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, const int64_t* __restrict__ mapping,
+    int64_t vec_per_block, int NB, int* err) {
+    const int p = blockIdx.x;
+    const int64_t src = mapping[2 * p], dst = mapping[2 * p + 1];
+    if (src < 0 || src >= NB || dst < 0 || dst >= NB) {
+        if (threadIdx.x == 0 && blockIdx.y == 0) pkv::report(err, PKV_DEVERR_BLOCK_ID);
+        return;
+    }
+    const int64_t per = (vec_per_block + gridDim.y - 1) / gridDim.y;
+    const int64_t lo = blockIdx.y * per;
+    const int64_t hi = lo + per < vec_per_block ? lo + per : vec_per_block;
+    const uint4* ks = k_cache + src * vec_per_block;
+    const uint4* vs = v_cache + src * vec_per_block;
+    uint4* kd = k_cache + dst * vec_per_block;
+    uint4* vd = v_cache + dst * vec_per_block;
+    for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+        uint4 a = ks[i];
+        uint4 b = vs[i];
+        kd[i] = a;
+        vd[i] = b;
+    }
+}
+
+bool supported(int D, int bs) { return (D == 64 || D == 128) && (bs == 16 || bs == 32); }
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_compute_slot_mapping(int64_t* slot_mapping, const int32_t* block_tables,
+                                    const int32_t* seq_idx, const int32_t* pos, int T, int S,
+                                    int MB, int bs, void* stream) {
+    pkv::clear_error();
+    if (T < 0 || S < 0 || MB < 0 || bs <= 0)
+        return pkv::fail(PKV_ERR_INVALID_ARG, "compute_slot_mapping: bad size");
+    if (T == 0) return PKV_OK;
+    if (!slot_mapping || !seq_idx || !pos || (S > 0 && MB > 0 && !block_tables))
+        return pkv::fail(PKV_ERR_INVALID_ARG, "compute_slot_mapping: null pointer");
+    const int threads = 256;
+    slot_mapping_kernel<<<(T + threads - 1) / threads, threads, 0, pkv::as_stream(stream)>>>(
+        slot_mapping, block_tables, seq_idx, pos, T, S, MB, bs, pkv::device_error_word());
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? PKV_OK : pkv::cuda_fail(e, "compute_slot_mapping launch");
+}
+
+pkv_status pkv_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
+                                 const int64_t* slot_mapping, int T, int H, int D, int bs, int NB,
+                                 pkv_dtype dtype, void* stream) {
+    pkv::clear_error();
+    if (T < 0 || H <= 0 || NB < 0 || (dtype != PKV_F16 && dtype != PKV_BF16))
+        return pkv::fail(PKV_ERR_INVALID_ARG, "reshape_and_cache: bad size or dtype");
+    if (!supported(D, bs)) return pkv::fail(PKV_ERR_UNSUPPORTED, "reshape_and_cache: unsupported head_dim/block_size");
+    if (T == 0) return PKV_OK;
+    if (!key || !value || !k_cache || !v_cache || !slot_mapping)
+        return pkv::fail(PKV_ERR_INVALID_ARG, "reshape_and_cache: null pointer");
+    if (!pkv::aligned16(key) || !pkv::aligned16(value) || !pkv::aligned16(k_cache) || !pkv::aligned16(v_cache))
+        return pkv::fail(PKV_ERR_INVALID_ARG, "reshape_and_cache: pointers must be 16-byte aligned");
+    const int vec_per_row = H * D / 8;
+    const int threads = vec_per_row >= 256 ? 256 : ((vec_per_row + 31) / 32) * 32;
+    reshape_and_cache_kernel<<<T, threads, 0, pkv::as_stream(stream)>>>(
+        static_cast<const uint4*>(key), static_cast<const uint4*>(value), static_cast<uint4*>(k_cache),
+        static_cast<uint4*>(v_cache), slot_mapping, vec_per_row, (int64_t)NB * bs,
+        pkv::device_error_word());
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? PKV_OK : pkv::cuda_fail(e, "reshape_and_cache launch");
+}
+
+pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapping, int P,
+                           int H, int D, int bs, int NB, pkv_dtype dtype, void* stream) {
+    pkv::clear_error();
+    if (P < 0 || H <= 0 || NB < 0 || (dtype != PKV_F16 && dtype != PKV_BF16))
+        return pkv::fail(PKV_ERR_INVALID_ARG, "copy_blocks: bad size or dtype");
+    if (!supported(D, bs)) return pkv::fail(PKV_ERR_UNSUPPORTED, "copy_blocks: unsupported head_dim/block_size");
+    if (P == 0) return PKV_OK;
+    if (!k_cache || !v_cache || !block_mapping)
+        return pkv::fail(PKV_ERR_INVALID_ARG, "copy_blocks: null pointer");
+    if (!pkv::aligned16(k_cache) || !pkv::aligned16(v_cache))
+        return pkv::fail(PKV_ERR_INVALID_ARG, "copy_blocks: pointers must be 16-byte aligned");
+    if (P > 65535 * 64) return pkv::fail(PKV_ERR_INVALID_ARG, "copy_blocks: too many pairs");
+    const int64_t vec_per_block = (int64_t)bs * H * D / 8;
+    // ~2 KB of K and 2 KB of V per thread-row pass; 16 KB of each per CTA
+    int splits = (int)((vec_per_block + 1023) / 1024);
+    if (splits > 64) splits = 64;
+    if (splits < 1) splits = 1;
+    dim3 grid(P, splits);
+    copy_blocks_kernel<<<grid, 256, 0, pkv::as_stream(stream)>>>(
+        static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), block_mapping, vec_per_block, NB,
+        pkv::device_error_word());
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? PKV_OK : pkv::cuda_fail(e, "copy_blocks launch");
+}
+
+}  // extern "C"

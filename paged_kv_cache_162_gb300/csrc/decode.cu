@@ -1,0 +1,534 @@
+// Single-query paged decode attention for sm_103a.
+//
+// What it computes ("3.1 PagedAttention的核心原理" 3.1.3; notes on "vLLM: Easy,
+// Fast, and Cheap LLM Serving with PagedAttention", "疑问" 1): for every
+// sequence s and head h, out = softmax(scale * q K^T) V over the sequence's
+// context, each token's K/V row found through the block table (logical =
+// j / bs, offset = j % bs, physical = table[logical]).
+//
+// How (HBM-bound GEMV: 1 FMA per 16-bit element loaded, so no tensor cores):
+//  * A work item is (sequence, partition of `PT` tokens, group of 4 heads).
+//    The CTA has 4 warps, one per head; a warp streams its partition in
+//    16-token tiles.  Within a tile, lane (r, c) loads 16 bytes (8 dims,
+//    chunk c) of rows r, r + RPI, ... so every warp-wide load reads whole
+//    256-byte (D=128) or 128-byte (D=64) rows: coalesced 128-bit loads, and
+//    the 4 warps of a CTA together read 4 consecutive heads = 1 KB (512 B)
+//    of each token row.  Only tiles of one physical block are read together
+//    ("3.3 页面级显存管理" 3.3.1: work organised per physical block, reads
+//    within a block coalesced).
+//  * q.k: per-lane partial dots over 8 dims, then a reduce-scatter across
+//    the lanes of a row (log2(NI) halving steps + one xor-1 step) leaves each
+//    lane with the full logit of one row.  Online softmax in log2 units
+//    (q is pre-scaled by scale*log2(e)); P.V accumulates 8 dims per lane in
+//    fp32 and is combined across row groups once at the end.
+//  * Partitions: a context longer than PT tokens is split.  Each partition
+//    writes (running max, running sum, unnormalised output) to the
+//    workspace; the CTA that finishes a (sequence, head group) last -- known
+//    from an atomic ticket, no waiting -- merges them.  A single-partition
+//    context writes its output directly.
+//  * Scheduling: a one-CTA plan kernel lists the (sequence, partition)
+//    items, full partitions first and partial ones last, and resets the
+//    work counter and tickets.  The decode kernel is persistent (as many
+//    CTAs as fit on the SMs) and takes items from the counter, longest
+//    first, so the tail is at most one partition long.  It is launched with
+//    programmatic dependent launch so its CTAs are resident when the plan
+//    kernel ends.
+//  * Safety: a table entry outside [0, NB) or a context outside
+//    [0, max_context_len] is never dereferenced; the kernel masks it and
+//    sets a bit in the device error word.  No CTA ever waits on another.
+#include <cmath>
+#include <mutex>
+
+#include "pagedkv.h"
+#include "pkv_device.cuh"
+
+namespace {
+
+constexpr int kWarps = 4;                // heads per CTA, one warp per head
+constexpr int kThreads = 32 * kWarps;
+constexpr int kTile = 16;                // tokens per tile
+constexpr int kDefaultPartition = 256;   // tokens per split-K partition
+constexpr int kPlanThreads = 1024;
+constexpr unsigned kFull = 0xffffffffu;
+
+struct Workspace {
+    unsigned* counter;  // next work item
+    int* n_items;       // number of (sequence, partition) items
+    int* items;         // packed (sequence << 16 | partition)
+    int* nparts;        // partitions per sequence
+    unsigned* tickets;  // per (sequence, head group): partitions finished
+    float* m;           // [S][H][max_parts] running max (log2 units)
+    float* l;           // [S][H][max_parts] running sum
+    float* acc;         // [S][H][max_parts][D] unnormalised output
+};
+
+struct Layout {
+    size_t items, nparts, tickets, m, l, acc, total;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+Layout layout_of(int S, int H, int D, int max_parts) {
+    const size_t HG = (size_t)(H + kWarps - 1) / kWarps;
+    const size_t part_elems = (size_t)S * H * max_parts;
+    Layout L;
+    size_t o = 256;  // header: counter, n_items
+    L.items = o;   o = align256(o + (size_t)S * max_parts * sizeof(int));
+    L.nparts = o;  o = align256(o + (size_t)S * sizeof(int));
+    L.tickets = o; o = align256(o + (size_t)S * HG * sizeof(unsigned));
+    L.m = o;       o = align256(o + part_elems * sizeof(float));
+    L.l = o;       o = align256(o + part_elems * sizeof(float));
+    L.acc = o;     o = align256(o + part_elems * D * sizeof(float));
+    L.total = o;
+    return L;
+}
+
+Workspace bind(void* base, const Layout& L) {
+    char* b = static_cast<char*>(base);
+    Workspace w;
+    w.counter = reinterpret_cast<unsigned*>(b);
+    w.n_items = reinterpret_cast<int*>(b + 4);
+    w.items = reinterpret_cast<int*>(b + L.items);
+    w.nparts = reinterpret_cast<int*>(b + L.nparts);
+    w.tickets = reinterpret_cast<unsigned*>(b + L.tickets);
+    w.m = reinterpret_cast<float*>(b + L.m);
+    w.l = reinterpret_cast<float*>(b + L.l);
+    w.acc = reinterpret_cast<float*>(b + L.acc);
+    return w;
+}
+
+struct DecodeParams {
+    void* out;
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    int S, H, NB, MB, HG, PT, max_parts, max_ctx;
+    float qscale;  // scale * log2(e)
+    Workspace ws;
+    int* err;
+};
+
+__device__ __forceinline__ int clamp_ctx(int c, int max_ctx) {
+    return c < 0 ? 0 : (c > max_ctx ? max_ctx : c);
+}
+
+// ---------------------------------------------------------------------------
+// Plan: list the work items and reset the counter and the tickets.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __restrict__ context_lens,
+                                                             int S, int PT, int max_ctx, int HG,
+                                                             Workspace ws, int* err) {
+    // the decode kernel may launch now; it waits for this grid to finish
+    asm volatile("griddepcontrol.launch_dependents;");
+    __shared__ int warp_sum[2][32];
+    __shared__ int carry[2];
+    __shared__ int n_full_total;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    for (int pass = 0; pass < 2; ++pass) {
+        if (tid == 0) carry[0] = carry[1] = 0;
+        __syncthreads();
+        for (int base = 0; base < S; base += kPlanThreads) {
+            const int s = base + tid;
+            int nf = 0, np = 0;
+            if (s < S) {
+                int c = context_lens[s];
+                if (c < 0 || c > max_ctx) {
+                    if (pass == 0) pkv::report(err, PKV_DEVERR_CONTEXT);
+                    c = clamp_ctx(c, max_ctx);
+                }
+                nf = c / PT;
+                np = (c % PT != 0 || c == 0) ? 1 : 0;  // an empty context still writes zeros
+            }
+            int a = nf, b = np;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int x = __shfl_up_sync(kFull, a, o), y = __shfl_up_sync(kFull, b, o);
+                if (lane >= o) { a += x; b += y; }
+            }
+            if (lane == 31) { warp_sum[0][wid] = a; warp_sum[1][wid] = b; }
+            __syncthreads();
+            if (wid == 0) {
+                int x = warp_sum[0][lane], y = warp_sum[1][lane];
+                int xi = x, yi = y;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    int u = __shfl_up_sync(kFull, xi, o), v = __shfl_up_sync(kFull, yi, o);
+                    if (lane >= o) { xi += u; yi += v; }
+                }
+                warp_sum[0][lane] = xi - x;  // exclusive
+                warp_sum[1][lane] = yi - y;
+            }
+            __syncthreads();
+            const int incl_f = a + warp_sum[0][wid], incl_p = b + warp_sum[1][wid];
+            if (pass == 1 && s < S) {
+                const int off_f = carry[0] + incl_f - nf, off_p = carry[1] + incl_p - np;
+                for (int k = 0; k < nf; ++k) ws.items[off_f + k] = (s << 16) | k;
+                if (np) ws.items[n_full_total + off_p] = (s << 16) | nf;
+                ws.nparts[s] = nf + np;
+            }
+            __syncthreads();
+            if (tid == kPlanThreads - 1) { carry[0] += incl_f; carry[1] += incl_p; }
+            __syncthreads();
+        }
+        if (pass == 0 && tid == 0) n_full_total = carry[0];
+        __syncthreads();
+    }
+    for (int i = tid; i < S * HG; i += kPlanThreads) ws.tickets[i] = 0u;
+    if (tid == 0) {
+        *ws.counter = 0u;
+        *ws.n_items = carry[0] + carry[1];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// One warp: one head over one partition.
+// ---------------------------------------------------------------------------
+template <class E, int D, int BS>
+__device__ __forceinline__ void attend_partition(const DecodeParams& a, int s, int h, int part,
+                                                 int t_begin, int t_end, int np, int lane) {
+    constexpr int LPR = D / 8;         // lanes per row: 16 bytes each
+    constexpr int RPI = 32 / LPR;      // rows per warp-wide load
+    constexpr int NI = kTile / RPI;    // warp-wide loads per tile (K and V each)
+    const int r = lane / LPR, c = lane % LPR;
+    const int64_t HD = (int64_t)a.H * D;
+
+    float qf[8];
+    {
+        const uint4 qv = __ldg(reinterpret_cast<const uint4*>(
+            static_cast<const uint16_t*>(a.q) + ((int64_t)s * a.H + h) * D + c * 8));
+        pkv::unpack8<E>(qv, qf);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) qf[j] *= a.qscale;
+    }
+    const uint16_t* kb = static_cast<const uint16_t*>(a.k_cache) + (int64_t)h * D + c * 8;
+    const uint16_t* vb = static_cast<const uint16_t*>(a.v_cache) + (int64_t)h * D + c * 8;
+    const int32_t* bt_row = a.block_tables + (int64_t)s * a.MB;
+
+    float m_run = -INFINITY, l_run = 0.f;
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+
+    for (int t0 = t_begin; t0 < t_end; t0 += kTile) {
+        const int lb = t0 / BS;
+        const int off0 = t0 - lb * BS;
+        const int phys = __ldg(bt_row + lb);
+        const bool ok = (unsigned)phys < (unsigned)a.NB;
+        if (!ok && lane == 0) pkv::report(a.err, PKV_DEVERR_BLOCK_ID);
+        const int64_t row0 = (int64_t)(ok ? phys : 0) * BS + off0;
+
+        uint4 kr[NI], vr[NI];
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+            const int row = RPI * i + r;
+            const bool valid = ok && (t0 + row < t_end);
+            const int64_t off = (row0 + row) * HD;
+            kr[i] = valid ? pkv::ld_stream(kb + off) : make_uint4(0, 0, 0, 0);
+            vr[i] = valid ? pkv::ld_stream(vb + off) : make_uint4(0, 0, 0, 0);
+        }
+
+        // partial dots over this lane's 8 dims, one per loaded row
+        float pd[NI];
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+            float kf[8];
+            pkv::unpack8<E>(kr[i], kf);
+            float d = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) d = fmaf(qf[j], kf[j], d);
+            pd[i] = d;
+        }
+        // reduce-scatter across the LPR lanes of a row group: after the
+        // halving steps lane c holds row index c>>1 summed over half the
+        // lanes, the xor-1 step completes the sum
+#pragma unroll
+        for (int mask = LPR / 2, n = NI; mask >= 2; mask >>= 1, n >>= 1) {
+            const bool upper = (lane & mask) != 0;
+#pragma unroll
+            for (int j = 0; j < n / 2; ++j) {
+                const float send = upper ? pd[j] : pd[j + n / 2];
+                const float keep = upper ? pd[j + n / 2] : pd[j];
+                pd[j] = keep + __shfl_xor_sync(kFull, send, mask);
+            }
+        }
+        const float logit = pd[0] + __shfl_xor_sync(kFull, pd[0], 1);
+        const int own_row = RPI * (c >> 1) + r;
+        const float sc = (ok && t0 + own_row < t_end) ? logit : -INFINITY;
+
+        float mt = sc;
+#pragma unroll
+        for (int mask = 16; mask >= 2; mask >>= 1) mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, mask));
+        const float m_new = fmaxf(m_run, mt);
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        const float corr = exp2f(m_run - m_use);
+        const float p = exp2f(sc - m_use);
+        l_run = fmaf(l_run, corr, p);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] *= corr;
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+            const float pi = __shfl_sync(kFull, p, r * LPR + 2 * i);
+            float vf[8];
+            pkv::unpack8<E>(vr[i], vf);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] = fmaf(pi, vf[j], acc[j]);
+        }
+        m_run = m_new;
+    }
+
+    // combine the row groups; l over the 16 distinct rows of each tile
+#pragma unroll
+    for (int mask = LPR; mask < 32; mask <<= 1) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] += __shfl_xor_sync(kFull, acc[j], mask);
+    }
+#pragma unroll
+    for (int mask = 16; mask >= 2; mask >>= 1) l_run += __shfl_xor_sync(kFull, l_run, mask);
+
+    if (np == 1) {
+        if (lane < LPR) {
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] *= inv;
+            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + ((int64_t)s * a.H + h) * D +
+                                      c * 8) = pkv::pack8<E>(acc);
+        }
+    } else {
+        const int64_t idx = ((int64_t)s * a.H + h) * a.max_parts + part;
+        if (lane < LPR) {
+            float4* dst = reinterpret_cast<float4*>(a.ws.acc + idx * D + c * 8);
+            dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        }
+        if (lane == 0) {
+            a.ws.m[idx] = m_run;
+            a.ws.l[idx] = l_run;
+        }
+    }
+}
+
+// Merge the partitions of one (sequence, head): with M = max_p m_p,
+// out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p.
+template <class E, int D>
+__device__ __forceinline__ void merge_partitions(const DecodeParams& a, int s, int h, int np,
+                                                 int lane) {
+    constexpr int DPL = D / 32;  // dims per lane
+    const int64_t base = ((int64_t)s * a.H + h) * a.max_parts;
+    float M = -INFINITY;
+    for (int p = lane; p < np; p += 32) M = fmaxf(M, __ldcg(a.ws.m + base + p));
+#pragma unroll
+    for (int mask = 16; mask >= 1; mask >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, mask));
+    float L = 0.f;
+    for (int p = lane; p < np; p += 32) {
+        const float mp = __ldcg(a.ws.m + base + p);
+        if (mp != -INFINITY) L = fmaf(exp2f(mp - M), __ldcg(a.ws.l + base + p), L);
+    }
+#pragma unroll
+    for (int mask = 16; mask >= 1; mask >>= 1) L += __shfl_xor_sync(kFull, L, mask);
+
+    float o[DPL];
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) o[j] = 0.f;
+#pragma unroll 4
+    for (int p = 0; p < np; ++p) {
+        const float mp = __ldcg(a.ws.m + base + p);
+        const float w = (mp == -INFINITY) ? 0.f : exp2f(mp - M);
+        const float* src = a.ws.acc + (base + p) * D + lane * DPL;
+        if constexpr (DPL == 4) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
+            o[0] = fmaf(w, v.x, o[0]); o[1] = fmaf(w, v.y, o[1]);
+            o[2] = fmaf(w, v.z, o[2]); o[3] = fmaf(w, v.w, o[3]);
+        } else {
+            const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
+            o[0] = fmaf(w, v.x, o[0]); o[1] = fmaf(w, v.y, o[1]);
+        }
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    uint16_t* dst = static_cast<uint16_t*>(a.out) + ((int64_t)s * a.H + h) * D + lane * DPL;
+    if constexpr (DPL == 4) {
+        uint2 v;
+        v.x = E::from_float2(o[0] * inv, o[1] * inv);
+        v.y = E::from_float2(o[2] * inv, o[3] * inv);
+        *reinterpret_cast<uint2*>(dst) = v;
+    } else {
+        *reinterpret_cast<uint32_t*>(dst) = E::from_float2(o[0] * inv, o[1] * inv);
+    }
+}
+
+template <class E, int D, int BS>
+__global__ void __launch_bounds__(kThreads, 4) decode_kernel(DecodeParams a) {
+    // wait for the plan kernel (programmatic dependent launch)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    __shared__ int s_item;
+    __shared__ int s_last;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int total = *a.ws.n_items * a.HG;
+    if (threadIdx.x == 0) s_item = (int)atomicAdd(a.ws.counter, 1u);
+    __syncthreads();
+    int item = s_item;
+    while (item < total) {
+        int next = 0;
+        if (threadIdx.x == 0) next = (int)atomicAdd(a.ws.counter, 1u);  // used at the end
+        const int hg = item % a.HG;
+        const int packed = a.ws.items[item / a.HG];
+        const int s = packed >> 16, part = packed & 0xffff;
+        const int np = a.ws.nparts[s];
+        const int ctx = clamp_ctx(a.context_lens[s], a.max_ctx);
+        const int t_begin = part * a.PT;
+        const int t_end = min(t_begin + a.PT, ctx);
+        const int h = hg * kWarps + warp;
+        if (h < a.H) attend_partition<E, D, BS>(a, s, h, part, t_begin, t_end, np, lane);
+        if (np > 1) {
+            __threadfence();
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                const unsigned done = atomicAdd(&a.ws.tickets[s * a.HG + hg], 1u);
+                s_last = (done == (unsigned)(np - 1)) ? 1 : 0;
+            }
+            __syncthreads();
+            if (s_last) {
+                __threadfence();
+                if (h < a.H) merge_partitions<E, D>(a, s, h, np, lane);
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) s_item = next;
+        __syncthreads();
+        item = s_item;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+using KernelFn = void (*)(DecodeParams);
+
+template <class E, int D>
+KernelFn pick_bs(int bs) {
+    return bs == 16 ? decode_kernel<E, D, 16> : decode_kernel<E, D, 32>;
+}
+
+template <class E>
+KernelFn pick_d(int D, int bs) {
+    return D == 64 ? pick_bs<E, 64>(bs) : pick_bs<E, 128>(bs);
+}
+
+KernelFn pick(pkv_dtype dt, int D, int bs) {
+    return dt == PKV_BF16 ? pick_d<pkv::BF16>(D, bs) : pick_d<pkv::F16>(D, bs);
+}
+
+int resident_ctas(KernelFn fn) {
+    static std::mutex mu;
+    static struct { KernelFn fn; int dev; int n; } cache[64];
+    static int used = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < used; ++i)
+        if (cache[i].fn == fn && cache[i].dev == dev) return cache[i].n;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, 0) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        n = 1;
+    }
+    if (used < 64) cache[used++] = {fn, dev, n};
+    return n;
+}
+
+int max_parts_of(int max_ctx, int PT) {
+    int mp = (max_ctx + PT - 1) / PT;
+    return mp < 1 ? 1 : mp;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pkv_decode_workspace_size(int S, int H, int D, int max_context_len, int partition_tokens) {
+    const int PT = partition_tokens == 0 ? kDefaultPartition : partition_tokens;
+    if (S < 0 || H <= 0 || (D != 64 && D != 128) || max_context_len < 0 || PT <= 0 || PT % kTile)
+        return 0;
+    return layout_of(S, H, D, max_parts_of(max_context_len, PT)).total;
+}
+
+pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_cache,
+                                      const void* v_cache, const int32_t* block_tables,
+                                      const int32_t* context_lens, int S, int H, int D, int bs,
+                                      int NB, int MB, int max_context_len, float scale,
+                                      pkv_dtype dtype, int partition_tokens, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+    pkv::clear_error();
+    if (S < 0 || H <= 0 || NB <= 0 || MB <= 0 || (dtype != PKV_F16 && dtype != PKV_BF16))
+        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode: bad size or dtype");
+    if ((D != 64 && D != 128) || (bs != 16 && bs != 32))
+        return pkv::fail(PKV_ERR_UNSUPPORTED, "paged_attention_decode: head_dim must be 64/128, block_size 16/32");
+    if (S == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace)
+        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode: null pointer");
+    if (!pkv::aligned16(out) || !pkv::aligned16(q) || !pkv::aligned16(k_cache) || !pkv::aligned16(v_cache))
+        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode: token pointers must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode: workspace must be 256-byte aligned");
+    const int64_t cap = (int64_t)MB * bs;
+    const int max_ctx = max_context_len == 0 ? (int)(cap < INT32_MAX ? cap : INT32_MAX) : max_context_len;
+    if (max_ctx < 0 || max_ctx > cap)
+        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode: max_context_len must be in [0, MB*bs]");
+    const int PT = partition_tokens == 0 ? kDefaultPartition : partition_tokens;
+    if (PT <= 0 || PT % kTile != 0 || PT % bs != 0)
+        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode: partition_tokens must be a multiple of 16 and of block_size");
+    if (!(scale == scale) || std::isinf(scale))
+        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode: scale must be finite");
+    const int max_parts = max_parts_of(max_ctx, PT);
+    if (S > 32767 || max_parts > 65535)
+        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode: at most 32767 sequences and 65535 partitions");
+    const Layout L = layout_of(S, H, D, max_parts);
+    if (workspace_bytes < L.total)
+        return pkv::fail(PKV_ERR_WORKSPACE, "paged_attention_decode: workspace too small");
+
+    DecodeParams p;
+    p.out = out;
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.S = S;
+    p.H = H;
+    p.NB = NB;
+    p.MB = MB;
+    p.HG = (H + kWarps - 1) / kWarps;
+    p.PT = PT;
+    p.max_parts = max_parts;
+    p.max_ctx = max_ctx;
+    p.qscale = scale * 1.4426950408889634f;  // log2(e)
+    p.ws = bind(workspace, L);
+    p.err = pkv::device_error_word();
+
+    cudaStream_t st = pkv::as_stream(stream);
+    plan_kernel<<<1, kPlanThreads, 0, st>>>(context_lens, S, PT, max_ctx, p.HG, p.ws, p.err);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return pkv::cuda_fail(e, "paged_attention_decode plan launch");
+
+    KernelFn fn = pick(dtype, D, bs);
+    const int64_t upper = (int64_t)S * max_parts * p.HG;
+    const int64_t resident = (int64_t)resident_ctas(fn) * pkv::sm_count();
+    const int grid = (int)(upper < resident ? upper : resident);
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, fn, p);
+    if (e != cudaSuccess) return pkv::cuda_fail(e, "paged_attention_decode launch");
+    return PKV_OK;
+}
+
+}  // extern "C"

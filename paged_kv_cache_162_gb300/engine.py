@@ -1,0 +1,187 @@
+"""Tensor-level calls and one decode step over a paged KV cache.
+
+PyTorch supplies device memory and streams only; every step of the path
+runs in libpagedkv.so through the C ABI (see _lib.py).
+
+The step, in the order a serving loop runs it ("3.3 页面级显存管理" 3.3.2;
+"vLLM三大核心技术分页内存与共享解码", Copy-on-Write section):
+  host   make room for each sequence's new tokens (copy-on-write of shared
+         blocks, new blocks as the token count grows) -- `plan_step`
+  device copy_blocks -> compute_slot_mapping -> reshape_and_cache ->
+         paged_attention_decode
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+from . import _lib as L
+from .allocator import BlockAllocator, plan_step
+
+_DTYPES = {torch.float16: L.PKV_F16, torch.bfloat16: L.PKV_BF16}
+_TORCH = {"f16": torch.float16, "bf16": torch.bfloat16}
+
+
+def dtype_code(t: torch.dtype) -> int:
+    if t not in _DTYPES:
+        raise L.PkvError(L.PKV_ERR_UNSUPPORTED, f"dtype {t} (fp16 and bf16 only)")
+    return _DTYPES[t]
+
+
+def torch_dtype(name: str) -> torch.dtype:
+    return _TORCH[name]
+
+
+def workspace_size(S, H, D, max_context_len, partition_tokens=0) -> int:
+    return L.pkv_decode_workspace_size(S, H, D, max_context_len, partition_tokens)
+
+
+def new_workspace(S, H, D, max_context_len, partition_tokens=0, device="cuda") -> torch.Tensor:
+    n = workspace_size(S, H, D, max_context_len, partition_tokens)
+    if n == 0:
+        raise L.PkvError(L.PKV_ERR_INVALID_ARG, "bad workspace arguments")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale=None,
+                           max_context_len=0, partition_tokens=0, workspace=None, stream=None):
+    """out[s,h] = softmax(scale q[s,h] K^T) V over each sequence's paged context.
+
+    q, out: [S, H, D]; caches: [NB, bs, H, D]; block_tables [S, MB] int32;
+    context_lens [S] int32 (all on the device).
+    """
+    S, H, D = q.shape
+    NB, bs = k_cache.shape[0], k_cache.shape[1]
+    MB = block_tables.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if workspace is None:
+        workspace = new_workspace(S, H, D, max_context_len or MB * bs, partition_tokens,
+                                  q.device)
+    L.pkv_paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, S, H, D, bs,
+                                 NB, MB, max_context_len, scale, dtype_code(q.dtype),
+                                 partition_tokens, workspace, workspace.numel(), stream)
+    return out
+
+
+def compute_slot_mapping(slot_mapping, block_tables, seq_idx, pos, block_size, stream=None):
+    L.pkv_compute_slot_mapping(slot_mapping, block_tables, seq_idx, pos, seq_idx.numel(),
+                               block_tables.shape[0], block_tables.shape[1], block_size, stream)
+    return slot_mapping
+
+
+def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, stream=None):
+    T, H, D = key.shape
+    NB, bs = k_cache.shape[0], k_cache.shape[1]
+    L.pkv_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, T, H, D, bs, NB,
+                            dtype_code(key.dtype), stream)
+
+
+def copy_blocks(k_cache, v_cache, block_mapping, stream=None):
+    NB, bs, H, D = k_cache.shape
+    P = block_mapping.shape[0] if block_mapping is not None else 0
+    L.pkv_copy_blocks(k_cache, v_cache, block_mapping, P, H, D, bs, NB,
+                      dtype_code(k_cache.dtype), stream)
+
+
+class DecodeStep:
+    """Device-resident state of one decode step and the calls that run it.
+
+    Built from plain arrays (16-bit data as uint16 bit patterns):
+      caches: pool [NB, bs, H, D]; `blocks` lists the physical blocks whose
+              contents `k_blocks`/`v_blocks` give, every other slot is set
+              to `fill_bits`;
+      tables_pre/nblocks_pre/ctx_before: the sequences before the step;
+      n_new, new_k/new_v [T, H, D], seq_idx/pos [T]: the tokens appended;
+      initial_free: the free list (last element handed out first).
+    `plan()` runs the host allocator; `run()` launches copy_blocks, slot
+    mapping, reshape_and_cache and decode on `stream`.
+    """
+
+    def __init__(self, *, dtype: str, S, H, D, bs, NB, MB, scale, ctx_before, n_new, tables_pre,
+                 nblocks_pre, initial_free, blocks, k_blocks, v_blocks, q, new_k, new_v, seq_idx,
+                 pos, fill_bits: int, partition_tokens: int = 0, device="cuda"):
+        self.dtype = torch_dtype(dtype)
+        self.S, self.H, self.D, self.bs, self.NB, self.MB = S, H, D, bs, NB, MB
+        self.scale = float(scale)
+        self.partition_tokens = partition_tokens
+        self.device = torch.device(device)
+        self.ctx_before = np.asarray(ctx_before, dtype=np.int32)
+        self.n_new = np.asarray(n_new, dtype=np.int32)
+        self.context_lens_host = (self.ctx_before + self.n_new).astype(np.int32)
+        self.tables_pre = np.asarray(tables_pre, dtype=np.int32)
+        self.nblocks_pre = np.asarray(nblocks_pre, dtype=np.int32)
+        self.initial_free = np.asarray(initial_free, dtype=np.int32)
+        self.max_context_len = max(int(self.context_lens_host.max(initial=0)), 1)
+        dev = self.device
+
+        def up16(a):
+            t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16))
+            return t.to(dev).view(self.dtype)
+
+        self.k_cache = torch.empty((NB, bs, H, D), dtype=torch.int16, device=dev)
+        self.v_cache = torch.empty((NB, bs, H, D), dtype=torch.int16, device=dev)
+        fill = int(np.int16(np.uint16(fill_bits)))
+        self.k_cache.fill_(fill)
+        self.v_cache.fill_(fill)
+        if len(blocks):
+            idx = torch.from_numpy(np.asarray(blocks, dtype=np.int64)).to(dev)
+            for dst, src in ((self.k_cache, k_blocks), (self.v_cache, v_blocks)):
+                chunk = 2048
+                for i in range(0, len(blocks), chunk):
+                    part = torch.from_numpy(np.ascontiguousarray(src[i:i + chunk]).view(np.int16))
+                    dst.index_copy_(0, idx[i:i + chunk], part.to(dev))
+        self.k_cache = self.k_cache.view(self.dtype)
+        self.v_cache = self.v_cache.view(self.dtype)
+        self.q = up16(q)
+        self.new_k = up16(new_k)
+        self.new_v = up16(new_v)
+        self.seq_idx = torch.from_numpy(np.asarray(seq_idx, dtype=np.int32)).to(dev)
+        self.pos = torch.from_numpy(np.asarray(pos, dtype=np.int32)).to(dev)
+        self.T = int(self.seq_idx.numel())
+        self.context_lens = torch.from_numpy(self.context_lens_host).to(dev)
+        self.slot_mapping = torch.empty(max(self.T, 1), dtype=torch.int64, device=dev)
+        self.out = torch.empty((S, H, D), dtype=self.dtype, device=dev)
+        self.workspace = new_workspace(S, H, D, self.max_context_len, partition_tokens, dev)
+        self.block_tables = None
+        self.pairs = None
+
+    def plan(self):
+        """Host allocator: tables and copy-on-write pairs for this step."""
+        self.allocator = BlockAllocator(self.NB, self.initial_free)
+        ids, counts = np.unique(self.tables_pre[self.tables_pre >= 0], return_counts=True)
+        for b, c in zip(ids.tolist(), counts.tolist()):
+            if c > 1:
+                self.allocator.incref([b] * (c - 1))
+        tables, nb, pairs = plan_step(self.allocator, self.tables_pre, self.nblocks_pre,
+                                      self.ctx_before, self.n_new, self.bs)
+        self.tables_host, self.nblocks_host, self.pairs_host = tables, nb, pairs
+        self.block_tables = torch.from_numpy(tables).to(self.device)
+        self.pairs = torch.from_numpy(np.ascontiguousarray(pairs)).to(self.device)
+        return tables, nb, pairs
+
+    def run(self, stream=None, attention=True, write=True):
+        """The device part of the step (all four kernels)."""
+        if self.block_tables is None:
+            self.plan()
+        if write:
+            if self.pairs.shape[0]:
+                copy_blocks(self.k_cache, self.v_cache, self.pairs, stream)
+            if self.T:
+                compute_slot_mapping(self.slot_mapping, self.block_tables, self.seq_idx, self.pos,
+                                     self.bs, stream)
+                reshape_and_cache(self.new_k, self.new_v, self.k_cache, self.v_cache,
+                                  self.slot_mapping, stream)
+        if attention:
+            self.decode(stream)
+        return self.out
+
+    def decode(self, stream=None):
+        L.pkv_paged_attention_decode(self.out, self.q, self.k_cache, self.v_cache,
+                                     self.block_tables, self.context_lens, self.S, self.H, self.D,
+                                     self.bs, self.NB, self.MB, self.max_context_len, self.scale,
+                                     dtype_code(self.dtype), self.partition_tokens, self.workspace,
+                                     self.workspace.numel(), stream)
+        return self.out

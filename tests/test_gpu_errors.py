@@ -1,0 +1,64 @@
+"""Out-of-range ids are never dereferenced: the kernels skip the access and
+set a bit in the device error word, which the host reads.  Every bad id
+below is caught by the kernels' own bounds checks."""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_162_gb300 as P
+from paged_kv_cache_162_gb300 import _lib as L
+from paged_kv_cache_162_gb300 import engine as E
+
+pytestmark = pytest.mark.gpu
+
+
+def _caches(NB=8, bs=16, H=4, D=64):
+    k = torch.randn(NB, bs, H, D, device="cuda").half()
+    v = torch.randn(NB, bs, H, D, device="cuda").half()
+    return k, v
+
+
+def test_bad_block_id_in_table_sets_flag_and_is_skipped():
+    P.pkv_get_device_errors()  # clear
+    k, v = _caches()
+    q = torch.randn(2, 4, 64, device="cuda").half()
+    out = torch.empty_like(q)
+    bt = torch.tensor([[0, 1], [2, 10_000]], dtype=torch.int32, device="cuda")
+    ctx = torch.tensor([20, 30], dtype=torch.int32, device="cuda")
+    E.paged_attention_decode(out, q, k, v, bt, ctx)
+    assert P.pkv_get_device_errors() & L.PKV_DEVERR_BLOCK_ID
+    assert torch.isfinite(out.float()).all()
+    assert P.pkv_get_device_errors() == 0  # cleared by the read
+
+
+def test_bad_context_len_is_clamped_and_flagged():
+    P.pkv_get_device_errors()
+    k, v = _caches()
+    q = torch.randn(1, 4, 64, device="cuda").half()
+    out = torch.empty_like(q)
+    bt = torch.tensor([[0, 1]], dtype=torch.int32, device="cuda")
+    ctx = torch.tensor([-5], dtype=torch.int32, device="cuda")
+    E.paged_attention_decode(out, q, k, v, bt, ctx)
+    assert P.pkv_get_device_errors() & L.PKV_DEVERR_CONTEXT
+    assert torch.all(out.float() == 0)
+
+
+def test_bad_slot_and_position_and_copy_pair():
+    P.pkv_get_device_errors()
+    k, v = _caches()
+    k0, v0 = k.clone(), v.clone()
+    key = torch.randn(2, 4, 64, device="cuda").half()
+    slots = torch.tensor([8 * 16, -1], dtype=torch.int64, device="cuda")  # first is one past the end
+    E.reshape_and_cache(key, key, k, v, slots)
+    assert P.pkv_get_device_errors() & L.PKV_DEVERR_SLOT
+    assert torch.equal(k, k0) and torch.equal(v, v0)
+    bt = torch.tensor([[0, 1]], dtype=torch.int32, device="cuda")
+    out = torch.empty(2, dtype=torch.int64, device="cuda")
+    E.compute_slot_mapping(out, bt, torch.tensor([0, 3], dtype=torch.int32, device="cuda"),
+                           torch.tensor([40, 1], dtype=torch.int32, device="cuda"), 16)
+    assert P.pkv_get_device_errors() & L.PKV_DEVERR_POSITION
+    assert out.tolist() == [-1, -1]
+    pairs = torch.tensor([[0, 8]], dtype=torch.int64, device="cuda")
+    E.copy_blocks(k, v, pairs)
+    assert P.pkv_get_device_errors() & L.PKV_DEVERR_BLOCK_ID
+    assert torch.equal(k, k0)

@@ -1,0 +1,108 @@
+"""GPU parity: the CUDA library against the fp64 oracle, through the C ABI.
+
+Bit-exact: block tables, copy-on-write pairs, slot mapping, both caches
+(every block the step may touch, plus a check that no other block changed).
+Attention: |gpu - oracle| <= 2e-3 + 1e-2 |oracle| per element.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from tests.gpu_harness import compare_step, device_step, out_to_double
+from oracle import step as OS
+
+pytestmark = pytest.mark.gpu
+
+
+def test_tiny_workload():
+    r = compare_step(W.tiny())
+    assert r["max_abs"] < 2e-3
+
+
+@pytest.mark.parametrize("dtype", [W.F16, W.BF16])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("bs", [16, 32])
+@pytest.mark.parametrize("pt", [32, 64, 256])
+def test_small_cases_span_tiles_partitions_and_ragged_tails(dtype, D, bs, pt):
+    # 6 heads: the second head group has 2 idle warps
+    w = W.small_case(seed=D * 1000 + bs * 10 + pt + (dtype == W.BF16) * 7, dtype=dtype, S=5, H=6, D=D, bs=bs,
+                     ctx_lo=1, ctx_hi=300, n_new=3)
+    compare_step(w, partition_tokens=pt)
+
+
+@pytest.mark.parametrize("ctx", [[0, 5, 0], [1, 1, 1], [16, 32, 48], [255, 256, 257], [512, 1, 513]])
+def test_edge_context_lengths(ctx):
+    w = W.small_case(seed=sum(ctx), S=3, H=4, D=128, bs=16, ctx=ctx, n_new=1, NB=120)
+    r = compare_step(w, partition_tokens=256)
+    out = out_to_double(r["step"].out)
+    for s, c in enumerate(ctx):
+        if c == 0:
+            assert np.all(out[s] == 0.0)
+
+
+def test_output_independent_of_partition_size():
+    w = W.small_case(seed=77, S=4, H=8, D=128, bs=16, ctx_lo=200, ctx_hi=900)
+    outs = []
+    for pt in (16, 64, 256, 1024):
+        st = device_step(w, pt)
+        st.run()
+        outs.append(out_to_double(st.out))
+    for o in outs[1:]:
+        np.testing.assert_allclose(o, outs[0], atol=2e-3, rtol=1e-2)
+
+
+def test_placement_invariance_bit_identical():
+    """Same logical K/V in two different physical placements."""
+    w1 = W.small_case(seed=5, S=4, H=4, D=128, bs=16, ctx_lo=50, ctx_hi=600, NB=200)
+    w2 = W.small_case(seed=5, S=4, H=4, D=128, bs=16, ctx_lo=50, ctx_hi=600, NB=200)
+    rng = np.random.default_rng(9)
+    perm = rng.permutation(w2.NB).astype(np.int32)
+    w2.tables_pre = np.where(w2.tables_pre >= 0, perm[np.maximum(w2.tables_pre, 0)], -1).astype(np.int32)
+    w2.blocks = perm[w1.blocks]
+    order = np.argsort(w2.blocks)
+    w2.blocks, w2.k_blocks, w2.v_blocks = w2.blocks[order], w1.k_blocks[order], w1.v_blocks[order]
+    w2.initial_free = perm[w1.initial_free]
+    outs = []
+    for w in (w1, w2):
+        st = device_step(w, 128)
+        st.run()
+        outs.append(st.out.cpu())
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
+
+def test_repeated_calls_are_deterministic():
+    w = W.small_case(seed=3, S=6, H=8, D=128, bs=16, ctx_lo=300, ctx_hi=2000)
+    st = device_step(w, 128)
+    st.run()
+    a = st.out.clone()
+    for _ in range(3):
+        st.decode()
+    assert torch.equal(a.view(torch.int16), st.out.view(torch.int16))
+
+
+# ------------------------------------------------ full-size workloads
+def test_llama7b_batch64_full():
+    r = compare_step(W.llama7b_batch64())
+    print("llama7b_batch64 max abs", r["max_abs"])
+
+
+def test_continuous_batching_bf16_full():
+    r = compare_step(W.continuous_batching_bf16())
+    print("continuous_batching_bf16 max abs", r["max_abs"], "max rel", r["max_rel"])
+
+
+def test_shared_prefix_full():
+    r = compare_step(W.shared_prefix())
+    assert r["pairs"] == 0
+
+
+def test_shared_prefix_cow_full():
+    r = compare_step(W.shared_prefix(cow=True))
+    assert r["pairs"] == 32 * 7
+
+
+@pytest.mark.parametrize("bs", [16, 32])
+def test_long_context_full(bs):
+    r = compare_step(W.long_context(bs=bs))
+    print(f"long_context_bs{bs} max abs", r["max_abs"])

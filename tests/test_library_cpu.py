@@ -1,0 +1,205 @@
+"""Host-side tests of libpagedkv.so that need no GPU: every symbol the header
+declares is exported, argument checks reject bad calls before any launch,
+and the C++ block allocator matches the oracle's allocator model."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import paged_kv_cache_162_gb300 as P
+from paged_kv_cache_162_gb300 import _lib as L
+from paged_kv_cache_162_gb300.allocator import BlockAllocator, OutOfBlocks
+from oracle.allocator import BlockAllocatorModel, OutOfBlocks as ModelOOM
+from tests.trace_replay import check_expect, load_traces, replay
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            text = open(os.path.join(inc, f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(pkv_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_library_exports_every_declared_symbol():
+    names = header_functions()
+    assert len(names) >= 20
+    lib = L.lib()
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in L.SIGNATURES, f"binding lacks {n}"
+
+
+def test_version_and_workspace_size():
+    assert "sm_103a" in P.pkv_version()
+    ws = P.pkv_decode_workspace_size(64, 32, 128, 2048, 256)
+    # at least the fp32 partials: S*H*parts*(D+2)*4 bytes
+    assert ws >= 64 * 32 * 8 * 130 * 4
+    assert P.pkv_decode_workspace_size(64, 32, 96, 2048, 256) == 0   # head_dim 96 not built
+    assert P.pkv_decode_workspace_size(64, 32, 128, 2048, 24) == 0   # not a multiple of 16
+    assert P.pkv_decode_workspace_size(0, 32, 128, 2048, 0) > 0
+
+
+def _decode_args(**kw):
+    a = dict(out=16, q=16, k_cache=16, v_cache=16, block_tables=16, context_lens=16, S=2, H=4,
+             D=128, bs=16, NB=8, MB=4, max_context_len=0, scale=0.1, dtype=L.PKV_F16,
+             partition_tokens=0, workspace=256, workspace_bytes=1 << 30, stream=0)
+    a.update(kw)
+    return a
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=96), L.PKV_ERR_UNSUPPORTED),
+    (dict(bs=8), L.PKV_ERR_UNSUPPORTED),
+    (dict(dtype=7), L.PKV_ERR_INVALID_ARG),
+    (dict(q=0), L.PKV_ERR_INVALID_ARG),
+    (dict(out=18), L.PKV_ERR_INVALID_ARG),          # misaligned
+    (dict(workspace=272), L.PKV_ERR_INVALID_ARG),   # workspace not 256-aligned
+    (dict(workspace_bytes=100), L.PKV_ERR_WORKSPACE),
+    (dict(max_context_len=65), L.PKV_ERR_INVALID_ARG),  # > MB*bs
+    (dict(partition_tokens=40), L.PKV_ERR_INVALID_ARG),
+    (dict(bs=32, partition_tokens=48), L.PKV_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), L.PKV_ERR_INVALID_ARG),
+    (dict(H=0), L.PKV_ERR_INVALID_ARG),
+])
+def test_decode_rejects_bad_arguments_before_launch(kw, status):
+    a = _decode_args(**kw)
+    with pytest.raises(L.PkvError) as e:
+        P.pkv_paged_attention_decode(**a)
+    assert e.value.status == status
+    assert P.pkv_last_error_string()
+
+
+def test_decode_with_no_sequences_is_a_noop():
+    P.pkv_paged_attention_decode(**_decode_args(S=0, out=0, q=0))
+
+
+def test_cache_ops_reject_bad_arguments():
+    with pytest.raises(L.PkvError) as e:
+        P.pkv_reshape_and_cache(16, 16, 16, 16, 16, 4, 4, 80, 16, 8, L.PKV_F16, 0)
+    assert e.value.status == L.PKV_ERR_UNSUPPORTED
+    with pytest.raises(L.PkvError) as e:
+        P.pkv_reshape_and_cache(16, 0, 16, 16, 16, 4, 4, 64, 16, 8, L.PKV_F16, 0)
+    assert e.value.status == L.PKV_ERR_INVALID_ARG
+    with pytest.raises(L.PkvError) as e:
+        P.pkv_copy_blocks(16, 24, 16, 3, 4, 64, 16, 8, L.PKV_F16, 0)
+    assert e.value.status == L.PKV_ERR_INVALID_ARG
+    with pytest.raises(L.PkvError):
+        P.pkv_compute_slot_mapping(16, 16, 0, 16, 4, 1, 4, 16, 0)
+    # empty work is a no-op that touches nothing
+    P.pkv_reshape_and_cache(0, 0, 0, 0, 0, 0, 4, 64, 16, 8, L.PKV_F16, 0)
+    P.pkv_copy_blocks(0, 0, 0, 0, 4, 64, 16, 8, L.PKV_F16, 0)
+    P.pkv_compute_slot_mapping(0, 0, 0, 0, 0, 1, 4, 16, 0)
+
+
+# ------------------------------------------------------------- allocator
+@pytest.mark.parametrize("trace", [t for t in load_traces() if t["policy"] == "lifo"],
+                         ids=lambda t: t["name"])
+def test_library_allocator_replays_page_traces(trace):
+    a = BlockAllocator(trace["num_blocks"])
+    tables, log = replay(trace, a, OutOfBlocks)
+    check_expect(trace, a, tables, log)
+
+
+def test_library_allocator_matches_model_on_random_ops():
+    """Random alloc / share / append (with CoW) / release / cow sequences:
+    ids, copy pairs, refcounts and the free count agree after every op."""
+    rng = np.random.default_rng(123)
+    NB, bs = 300, 16
+    perm = rng.permutation(NB)
+    held0 = perm[:40]
+    free0 = perm[40:]
+    lib_a = BlockAllocator(NB, initial_free=free0)
+    mod_a = BlockAllocatorModel(NB, initial_free=free0)
+    tables = {0: [int(b) for b in held0[:20]], 1: [int(b) for b in held0[20:]]}
+    ctx = {0: 20 * bs - 3, 1: 20 * bs}
+    nxt = 2
+    for step in range(4000):
+        op = int(rng.integers(0, 6))
+        keys = list(tables)
+        outcome = []
+        for a, oom in ((lib_a, OutOfBlocks), (mod_a, ModelOOM)):
+            t2 = {k: list(v) for k, v in tables.items()}
+            try:
+                if op == 0:
+                    n = int(rng.integers(0, 5)) if a is lib_a else n
+                    res = a.alloc(n)
+                elif op == 1 and keys:
+                    r = keys[int(rng.integers(len(keys)))] if a is lib_a else r
+                    k = int(rng.integers(1, 40)) if a is lib_a else k
+                    res = (a.append(t2[r], ctx[r], k, bs), t2[r])
+                elif op == 2 and keys:
+                    r = keys[int(rng.integers(len(keys)))] if a is lib_a else r
+                    a.incref(t2[r])
+                    res = "shared"
+                elif op == 3 and keys:
+                    r = keys[int(rng.integers(len(keys)))] if a is lib_a else r
+                    res = a.decref(t2[r])
+                elif op == 4 and keys:
+                    r = keys[int(rng.integers(len(keys)))] if a is lib_a else r
+                    j = int(rng.integers(len(t2[r]))) if (a is lib_a and t2[r]) else (j if t2[r] else 0)
+                    res = a.cow(t2[r][j]) if t2[r] else None
+                else:
+                    res = None
+            except oom:
+                res = "oom"
+            outcome.append((res, a.num_free, a.num_shared, t2))
+        (r1, f1, s1, t1), (r2, f2, s2, _) = outcome
+        assert r1 == r2 and f1 == f2 and s1 == s2, (step, op, outcome)
+        # apply the op to the harness's view of the tables
+        if op == 0 and r1 != "oom":
+            tables[nxt] = list(r1)
+            ctx[nxt] = len(r1) * bs
+            nxt += 1
+        elif op == 1 and keys and r1 != "oom":
+            tables[r] = t1[r]
+            ctx[r] += k
+        elif op == 2 and keys:
+            tables[nxt] = list(tables[r])
+            ctx[nxt] = ctx[r]
+            nxt += 1
+        elif op == 3 and keys:
+            del tables[r]
+            del ctx[r]
+        elif op == 4 and keys and r1 not in ("oom", None):
+            new, copied = r1
+            if copied:
+                # the writer now holds `new` instead of the shared block
+                tables[r][j] = new
+        for b in range(0, NB, 7):
+            assert lib_a.refcount(b) == mod_a.refcount(b)
+
+
+def test_library_allocator_errors_change_nothing():
+    a = BlockAllocator(8)
+    ids = a.alloc(3)
+    with pytest.raises(OutOfBlocks):
+        a.alloc(6)
+    assert a.num_free == 5
+    with pytest.raises(L.PkvError):
+        a.decref([ids[0], ids[0]])          # held once, released twice
+    assert a.refcount(ids[0]) == 1 and a.num_free == 5
+    with pytest.raises(L.PkvError):
+        a.incref([ids[0], 99])
+    assert a.refcount(ids[0]) == 1
+    t = list(ids)
+    a.incref(t)
+    with pytest.raises(OutOfBlocks):
+        a.append(t, 40, 100, 16)             # needs 2 CoW copies + 7 blocks, 5 free
+    assert t == ids and a.num_free == 5 and a.refcount(ids[2]) == 2
+    with pytest.raises(L.PkvError):
+        BlockAllocator(4, initial_free=[0, 0])
+
+
+def test_library_allocator_create_with_order_pops_last_first():
+    a = BlockAllocator(10, initial_free=[3, 8, 1])
+    assert a.num_free == 3 and a.refcount(0) == 1 and a.refcount(3) == 0
+    assert a.alloc(2) == [1, 8]
+    assert a.decref([0]) == 1 and a.alloc(1) == [0]
