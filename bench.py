@@ -42,7 +42,7 @@ DECODE_SOURCES = ["paged_kv_cache_162_gb300/csrc/decode.cu",
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--steps", type=int, default=5000)
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="llama7b_batch64")
@@ -130,16 +130,19 @@ class ClockSampler:
             if len(f) < 9:
                 continue
             try:
-                rows.append((float(f[1]), float(f[2]), f[5:9]))
+                rows.append((float(f[1]), float(f[2]), f[5:9], float(f[3])))
             except ValueError:
                 continue
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
-        sms = sorted(r[0] for r in rows)
+        # samples under load: power within half of the highest seen
+        pmax = max(r[3] for r in rows)
+        load = [r for r in rows if r[3] >= 0.5 * pmax] or rows
+        sms = sorted(r[0] for r in load)
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2]) if v == "Active"})
+        reasons = sorted({names[i] for r in load for i, v in enumerate(r[2]) if v == "Active"})
         return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(load), "power_w_max": pmax}
 
 
 # ------------------------------------------------------------- workloads
@@ -212,9 +215,13 @@ def time_oracle(w, seconds_per_step=2.0):
     def one():
         run_items(items, tok)
 
-    t0 = time.perf_counter()
-    one()
-    dt = time.perf_counter() - t0
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        one()
+        reps += 1
+        if time.perf_counter() - t0 >= min(1.0, seconds_per_step):
+            break
+    dt = (time.perf_counter() - t0) / reps
     return dt, sample_bytes, n / w.H, threads, one
 
 
@@ -319,7 +326,7 @@ def run_ours(args):
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
-        time.sleep(0.05)
+        time.sleep(0.3)
         with torch.cuda.stream(stream):
             t_start.record(stream)
             for i in range(K):
