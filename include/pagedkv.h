@@ -117,6 +117,40 @@ pkv_status pkv_paged_attention_decode(
     float scale, pkv_dtype dtype, int partition_tokens,
     void* workspace, size_t workspace_bytes, void* stream);
 
+/* Size of the scratch array built into the library for
+ * pkv_paged_attention_decode_noalloc: 16 MiB per device. */
+#define PKV_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* Decode attention for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart: this is a deployment convenience.  Some
+ * callers may not call cudaMalloc at all: a plugin inside a serving runtime
+ * that owns every byte of device memory and hands it out only through its
+ * own pool, a latency-critical loop where a cudaMalloc could synchronise
+ * the whole device, or a small C host program with no device allocator of
+ * its own.  This entry point computes exactly what
+ * pkv_paged_attention_decode computes, with the same arguments except the
+ * workspace, and allocates nothing (no cudaMalloc, no cudaFree).
+ *
+ * Its split-K scratch is a static device array of PKV_NOALLOC_SCRATCH_BYTES
+ * inside the library: every GPU that loads the library holds one copy until
+ * the process exits.  A call whose scratch need (pkv_decode_workspace_size
+ * of the same S, H, D, max_context_len, partition_tokens) exceeds it
+ * returns PKV_ERR_WORKSPACE; use pkv_paged_attention_decode with a caller
+ * workspace for such sizes.
+ *
+ * The first call on a device looks up the array's device address with that
+ * device current; make that first call before any stream capture begins.
+ * All calls on a device share the one array, which keeps the last call's
+ * contents; each call resets what it reads before reading it.  Calls that
+ * overlap on the GPU (other streams, other host threads) race on the array
+ * and give wrong results: serialise them. */
+pkv_status pkv_paged_attention_decode_noalloc(
+    void* out, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, const int32_t* context_lens,
+    int S, int H, int D, int bs, int NB, int MB, int max_context_len,
+    float scale, pkv_dtype dtype, int partition_tokens, void* stream);
+
 /* ------------------------------------------------------------------ *
  * Cache maintenance kernels
  * ------------------------------------------------------------------ */

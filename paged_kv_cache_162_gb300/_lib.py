@@ -27,6 +27,7 @@ PKV_DEVERR_BLOCK_ID = 0x1
 PKV_DEVERR_SLOT = 0x2
 PKV_DEVERR_CONTEXT = 0x4
 PKV_DEVERR_POSITION = 0x8
+PKV_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
                  3: "PKV_ERR_OOM", 4: "PKV_ERR_WORKSPACE", 5: "PKV_ERR_CUDA"}
@@ -55,6 +56,8 @@ SIGNATURES = {
     "pkv_decode_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "pkv_paged_attention_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
                                         _I, _P, _SZ, _P]),
+    "pkv_paged_attention_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                                _I, _F, _I, _I, _P]),
     "pkv_compute_slot_mapping": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "pkv_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "pkv_copy_blocks": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
@@ -143,6 +146,17 @@ def pkv_paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_l
         ptr(out), ptr(q), ptr(k_cache), ptr(v_cache), ptr(block_tables), ptr(context_lens), S, H,
         D, bs, NB, MB, max_context_len, float(scale), int(dtype), partition_tokens, ptr(workspace),
         int(workspace_bytes), stream_handle(stream)), "paged_attention_decode")
+
+
+def pkv_paged_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, S, H,
+                                       D, bs, NB, MB, max_context_len, scale, dtype,
+                                       partition_tokens, stream=None) -> None:
+    """Decode attention with the library's built-in scratch array instead of
+    a caller workspace, for callers that may not allocate device memory."""
+    check(lib().pkv_paged_attention_decode_noalloc(
+        ptr(out), ptr(q), ptr(k_cache), ptr(v_cache), ptr(block_tables), ptr(context_lens), S, H,
+        D, bs, NB, MB, max_context_len, float(scale), int(dtype), partition_tokens,
+        stream_handle(stream)), "paged_attention_decode_noalloc")
 
 
 def pkv_compute_slot_mapping(slot_mapping, block_tables, seq_idx, pos, T, S, MB, bs,

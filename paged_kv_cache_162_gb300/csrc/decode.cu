@@ -37,6 +37,7 @@
 //    [0, max_context_len] is never dereferenced; the kernel masks it and
 //    sets a bit in the device error word.  No CTA ever waits on another.
 #include <cmath>
+#include <cstdio>
 #include <mutex>
 
 #include "pagedkv.h"
@@ -532,3 +533,130 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_ca
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode for callers that cannot allocate device memory.  The split-K
+// scratch is this file's static device array instead of a caller workspace.
+// ---------------------------------------------------------------------------
+
+// One copy per device that loads the library, held until the process exits.
+// Host code must not use this name as a device address (on the host it is a
+// stand-in): the address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[PKV_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device with that device current.
+pkv_status noalloc_scratch(void** addr) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return pkv::cuda_fail(e, "paged_attention_decode_noalloc: cudaGetDevice");
+    if (dev < 0 || dev >= kNoAllocMaxDevices)
+        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode_noalloc: device ordinal above 63");
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p) {
+            cudaGetLastError();
+            return pkv::cuda_fail(e, "paged_attention_decode_noalloc: cudaGetSymbolAddress of the scratch array");
+        }
+        g_noalloc_addr[dev] = p;
+    }
+    *addr = g_noalloc_addr[dev];
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" pkv_status pkv_paged_attention_decode_noalloc(
+    void* out, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, const int32_t* context_lens, int S, int H, int D, int bs, int NB,
+    int MB, int max_context_len, float scale, pkv_dtype dtype, int partition_tokens,
+    void* stream) {
+    pkv::clear_error();
+    if (S < 0 || H <= 0 || NB <= 0 || MB <= 0 || (dtype != PKV_F16 && dtype != PKV_BF16))
+        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode_noalloc: bad size or dtype");
+    if ((D != 64 && D != 128) || (bs != 16 && bs != 32))
+        return pkv::fail(PKV_ERR_UNSUPPORTED, "paged_attention_decode_noalloc: head_dim must be 64/128, block_size 16/32");
+    if (S == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode_noalloc: null pointer");
+    if (!pkv::aligned16(out) || !pkv::aligned16(q) || !pkv::aligned16(k_cache) || !pkv::aligned16(v_cache))
+        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode_noalloc: token pointers must be 16-byte aligned");
+    const int64_t cap = (int64_t)MB * bs;
+    const int max_ctx = max_context_len == 0 ? (int)(cap < INT32_MAX ? cap : INT32_MAX) : max_context_len;
+    if (max_ctx < 0 || max_ctx > cap)
+        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode_noalloc: max_context_len must be in [0, MB*bs]");
+    const int PT = partition_tokens == 0 ? kDefaultPartition : partition_tokens;
+    if (PT <= 0 || PT % kTile != 0 || PT % bs != 0)
+        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode_noalloc: partition_tokens must be a multiple of 16 and of block_size");
+    if (!(scale == scale) || std::isinf(scale))
+        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode_noalloc: scale must be finite");
+    const int max_parts = max_parts_of(max_ctx, PT);
+    if (S > 32767 || max_parts > 65535)
+        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode_noalloc: at most 32767 sequences and 65535 partitions");
+    const Layout L = layout_of(S, H, D, max_parts);
+    if (L.total > (size_t)PKV_NOALLOC_SCRATCH_BYTES) {
+        char msg[256];
+        snprintf(msg, sizeof msg,
+                 "paged_attention_decode_noalloc: this size needs %zu bytes of scratch, more than the "
+                 "%u built into the library; call pkv_paged_attention_decode with a workspace",
+                 L.total, (unsigned)PKV_NOALLOC_SCRATCH_BYTES);
+        return pkv::fail(PKV_ERR_WORKSPACE, msg);
+    }
+    void* scratch = nullptr;
+    pkv_status st = noalloc_scratch(&scratch);
+    if (st != PKV_OK) return st;
+
+    DecodeParams p;
+    p.out = out;
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.S = S;
+    p.H = H;
+    p.NB = NB;
+    p.MB = MB;
+    p.HG = (H + kWarps - 1) / kWarps;
+    p.PT = PT;
+    p.max_parts = max_parts;
+    p.max_ctx = max_ctx;
+    p.qscale = scale * 1.4426950408889634f;  // log2(e)
+    p.ws = bind(scratch, L);
+    p.err = pkv::device_error_word();
+
+    // The plan kernel rewrites the work counter, the item list, the
+    // partition counts and the merge tickets at the start of every call;
+    // each partial is written before it is read, so the previous call's
+    // contents never reach the output.
+    cudaStream_t cs = pkv::as_stream(stream);
+    plan_kernel<<<1, kPlanThreads, 0, cs>>>(context_lens, S, PT, max_ctx, p.HG, p.ws, p.err);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return pkv::cuda_fail(e, "paged_attention_decode_noalloc plan launch");
+
+    KernelFn fn = pick(dtype, D, bs);
+    const int64_t upper = (int64_t)S * max_parts * p.HG;
+    const int64_t resident = (int64_t)resident_ctas(fn) * pkv::sm_count();
+    const int grid = (int)(upper < resident ? upper : resident);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = cs;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, fn, p);
+    if (e != cudaSuccess) return pkv::cuda_fail(e, "paged_attention_decode_noalloc launch");
+    return PKV_OK;
+}
