@@ -16,11 +16,17 @@
 //    of each token row.  Only tiles of one physical block are read together
 //    ("3.3 页面级显存管理" 3.3.1: work organised per physical block, reads
 //    within a block coalesced).
-//  * q.k: per-lane partial dots over 8 dims, then a reduce-scatter across
-//    the lanes of a row (log2(NI) halving steps + one xor-1 step) leaves each
-//    lane with the full logit of one row.  Online softmax in log2 units
-//    (q is pre-scaled by scale*log2(e)); P.V accumulates 8 dims per lane in
-//    fp32 and is combined across row groups once at the end.
+//  * q.k: per-lane partial dots over 8 dims with fp32-accumulating fma on
+//    the 16-bit operands themselves (the products are exact in fp32), then a
+//    reduce-scatter across the lanes of a row (log2(NI) halving steps + one
+//    xor-1 step) leaves each lane with the full logit of one row.  Online
+//    softmax in log2 units (logits scaled by scale*log2(e)); P.V
+//    accumulates 8 dims per lane in fp32 and is combined across row groups
+//    once at the end.
+//  * The tile loop is software-pipelined on the registers it already has:
+//    the V loads of tile t are in flight while q.K(t) is computed, the K
+//    loads of tile t+1 while P.V(t) is accumulated.  Full tiles take no
+//    per-row predicates.
 //  * Partitions: a context longer than PT tokens is split.  Each partition
 //    writes (running max, running sum, unnormalised output) to the
 //    workspace; the CTA that finishes a (sequence, head group) last -- known
@@ -186,6 +192,58 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
 // ---------------------------------------------------------------------------
 // One warp: one head over one partition.
 // ---------------------------------------------------------------------------
+
+// acc + q.k over 8 dims, both operands 16-bit: f16 x f16 (or bf16 x bf16)
+// products are exact in fp32 and each is added with one fp32 rounding
+// (fma with .f32 result and 16-bit sources), so no operand is converted.
+template <class E>
+__device__ __forceinline__ float dot8(const uint4& q, const uint4& k, float acc);
+
+template <>
+__device__ __forceinline__ float dot8<pkv::F16>(const uint4& q, const uint4& k, float acc) {
+    const uint32_t qw[4] = {q.x, q.y, q.z, q.w}, kw[4] = {k.x, k.y, k.z, k.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        asm("{.reg .b16 ql, qh, kl, kh;\n\t"
+            "mov.b32 {ql, qh}, %1;\n\t"
+            "mov.b32 {kl, kh}, %2;\n\t"
+            "fma.rn.f32.f16 %0, ql, kl, %0;\n\t"
+            "fma.rn.f32.f16 %0, qh, kh, %0;}"
+            : "+f"(acc)
+            : "r"(qw[j]), "r"(kw[j]));
+    return acc;
+}
+
+template <>
+__device__ __forceinline__ float dot8<pkv::BF16>(const uint4& q, const uint4& k, float acc) {
+    const uint32_t qw[4] = {q.x, q.y, q.z, q.w}, kw[4] = {k.x, k.y, k.z, k.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        asm("{.reg .b16 ql, qh, kl, kh;\n\t"
+            "mov.b32 {ql, qh}, %1;\n\t"
+            "mov.b32 {kl, kh}, %2;\n\t"
+            "fma.rn.f32.bf16 %0, ql, kl, %0;\n\t"
+            "fma.rn.f32.bf16 %0, qh, kh, %0;}"
+            : "+f"(acc)
+            : "r"(qw[j]), "r"(kw[j]));
+    return acc;
+}
+
+// Loads the lane's NI rows (r, r + RPI, ...) of a 16-token tile: rows at or
+// past `nvalid` are zero and not read.  A full tile takes no predicates.
+template <int NI, int RPI>
+__device__ __forceinline__ void load_tile(uint4 (&dst)[NI], const uint16_t* base, int64_t rstride,
+                                          int nvalid, int r) {
+    if (nvalid == kTile) {
+#pragma unroll
+        for (int i = 0; i < NI; ++i) dst[i] = pkv::ld_stream(base + i * rstride);
+    } else {
+#pragma unroll
+        for (int i = 0; i < NI; ++i)
+            dst[i] = (RPI * i + r < nvalid) ? pkv::ld_stream(base + i * rstride) : make_uint4(0, 0, 0, 0);
+    }
+}
+
 template <class E, int D, int BS>
 __device__ __forceinline__ void attend_partition(const DecodeParams& a, int s, int h, int part,
                                                  int t_begin, int t_end, int np, int lane) {
@@ -194,17 +252,13 @@ __device__ __forceinline__ void attend_partition(const DecodeParams& a, int s, i
     constexpr int NI = kTile / RPI;    // warp-wide loads per tile (K and V each)
     const int r = lane / LPR, c = lane % LPR;
     const int64_t HD = (int64_t)a.H * D;
+    const int64_t rstride = RPI * HD;  // elements between a lane's rows
 
-    float qf[8];
-    {
-        const uint4 qv = __ldg(reinterpret_cast<const uint4*>(
-            static_cast<const uint16_t*>(a.q) + ((int64_t)s * a.H + h) * D + c * 8));
-        pkv::unpack8<E>(qv, qf);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) qf[j] *= a.qscale;
-    }
-    const uint16_t* kb = static_cast<const uint16_t*>(a.k_cache) + (int64_t)h * D + c * 8;
-    const uint16_t* vb = static_cast<const uint16_t*>(a.v_cache) + (int64_t)h * D + c * 8;
+    const uint4 qv = __ldg(reinterpret_cast<const uint4*>(
+        static_cast<const uint16_t*>(a.q) + ((int64_t)s * a.H + h) * D + c * 8));
+    // row r of (physical block 0, offset 0), this lane's 8 dims
+    const uint16_t* kb = static_cast<const uint16_t*>(a.k_cache) + r * HD + (int64_t)h * D + c * 8;
+    const uint16_t* vb = static_cast<const uint16_t*>(a.v_cache) + r * HD + (int64_t)h * D + c * 8;
     const int32_t* bt_row = a.block_tables + (int64_t)s * a.MB;
 
     float m_run = -INFINITY, l_run = 0.f;
@@ -212,71 +266,77 @@ __device__ __forceinline__ void attend_partition(const DecodeParams& a, int s, i
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j] = 0.f;
 
-    for (int t0 = t_begin; t0 < t_end; t0 += kTile) {
+    // valid rows of the tile at t0 (0 if its block id is out of range) and
+    // its element offset in the cache
+    auto locate = [&](int t0, int& nvalid) -> int64_t {
         const int lb = t0 / BS;
-        const int off0 = t0 - lb * BS;
         const int phys = __ldg(bt_row + lb);
         const bool ok = (unsigned)phys < (unsigned)a.NB;
         if (!ok && lane == 0) pkv::report(a.err, PKV_DEVERR_BLOCK_ID);
-        const int64_t row0 = (int64_t)(ok ? phys : 0) * BS + off0;
+        nvalid = ok ? min(kTile, t_end - t0) : 0;
+        return ((int64_t)(ok ? phys : 0) * BS + (t0 - lb * BS)) * HD;
+    };
 
+    if (t_begin < t_end) {
+        // software pipeline: V(t) loads fly while q.K(t) is computed, K(t+1)
+        // loads fly while P.V(t) is accumulated
         uint4 kr[NI], vr[NI];
-#pragma unroll
-        for (int i = 0; i < NI; ++i) {
-            const int row = RPI * i + r;
-            const bool valid = ok && (t0 + row < t_end);
-            const int64_t off = (row0 + row) * HD;
-            kr[i] = valid ? pkv::ld_stream(kb + off) : make_uint4(0, 0, 0, 0);
-            vr[i] = valid ? pkv::ld_stream(vb + off) : make_uint4(0, 0, 0, 0);
-        }
+        int nv;
+        int64_t off = locate(t_begin, nv);
+        load_tile<NI, RPI>(kr, kb + off, rstride, nv, r);
+        load_tile<NI, RPI>(vr, vb + off, rstride, nv, r);
+        for (int t0 = t_begin;;) {
+            const int t1 = t0 + kTile;
+            const bool more = t1 < t_end;
+            int nv1 = 0;
+            const int64_t off1 = more ? locate(t1, nv1) : 0;
 
-        // partial dots over this lane's 8 dims, one per loaded row
-        float pd[NI];
+            // partial dots over this lane's 8 dims, one per loaded row
+            float pd[NI];
 #pragma unroll
-        for (int i = 0; i < NI; ++i) {
-            float kf[8];
-            pkv::unpack8<E>(kr[i], kf);
-            float d = 0.f;
+            for (int i = 0; i < NI; ++i) pd[i] = dot8<E>(qv, kr[i], 0.f);
+            if (more) load_tile<NI, RPI>(kr, kb + off1, rstride, nv1, r);
+            // reduce-scatter across the LPR lanes of a row group: after the
+            // halving steps lane c holds row index c>>1 summed over half the
+            // lanes, the xor-1 step completes the sum
 #pragma unroll
-            for (int j = 0; j < 8; ++j) d = fmaf(qf[j], kf[j], d);
-            pd[i] = d;
-        }
-        // reduce-scatter across the LPR lanes of a row group: after the
-        // halving steps lane c holds row index c>>1 summed over half the
-        // lanes, the xor-1 step completes the sum
+            for (int mask = LPR / 2, n = NI; mask >= 2; mask >>= 1, n >>= 1) {
+                const bool upper = (lane & mask) != 0;
 #pragma unroll
-        for (int mask = LPR / 2, n = NI; mask >= 2; mask >>= 1, n >>= 1) {
-            const bool upper = (lane & mask) != 0;
-#pragma unroll
-            for (int j = 0; j < n / 2; ++j) {
-                const float send = upper ? pd[j] : pd[j + n / 2];
-                const float keep = upper ? pd[j + n / 2] : pd[j];
-                pd[j] = keep + __shfl_xor_sync(kFull, send, mask);
+                for (int j = 0; j < n / 2; ++j) {
+                    const float send = upper ? pd[j] : pd[j + n / 2];
+                    const float keep = upper ? pd[j + n / 2] : pd[j];
+                    pd[j] = keep + __shfl_xor_sync(kFull, send, mask);
+                }
             }
-        }
-        const float logit = pd[0] + __shfl_xor_sync(kFull, pd[0], 1);
-        const int own_row = RPI * (c >> 1) + r;
-        const float sc = (ok && t0 + own_row < t_end) ? logit : -INFINITY;
+            const float logit = (pd[0] + __shfl_xor_sync(kFull, pd[0], 1)) * a.qscale;
+            const int own_row = RPI * (c >> 1) + r;
+            const float sc = own_row < nv ? logit : -INFINITY;
 
-        float mt = sc;
+            float mt = sc;
 #pragma unroll
-        for (int mask = 16; mask >= 2; mask >>= 1) mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, mask));
-        const float m_new = fmaxf(m_run, mt);
-        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        const float corr = exp2f(m_run - m_use);
-        const float p = exp2f(sc - m_use);
-        l_run = fmaf(l_run, corr, p);
+            for (int mask = 16; mask >= 2; mask >>= 1) mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, mask));
+            const float m_new = fmaxf(m_run, mt);
+            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+            const float corr = exp2f(m_run - m_use);
+            const float p = exp2f(sc - m_use);
+            l_run = fmaf(l_run, corr, p);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] *= corr;
+            for (int j = 0; j < 8; ++j) acc[j] *= corr;
 #pragma unroll
-        for (int i = 0; i < NI; ++i) {
-            const float pi = __shfl_sync(kFull, p, r * LPR + 2 * i);
-            float vf[8];
-            pkv::unpack8<E>(vr[i], vf);
+            for (int i = 0; i < NI; ++i) {
+                const float pi = __shfl_sync(kFull, p, r * LPR + 2 * i);
+                float vf[8];
+                pkv::unpack8<E>(vr[i], vf);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[j] = fmaf(pi, vf[j], acc[j]);
+                for (int j = 0; j < 8; ++j) acc[j] = fmaf(pi, vf[j], acc[j]);
+            }
+            m_run = m_new;
+            if (!more) break;
+            load_tile<NI, RPI>(vr, vb + off1, rstride, nv1, r);
+            t0 = t1;
+            nv = nv1;
         }
-        m_run = m_new;
     }
 
     // combine the row groups; l over the 16 distinct rows of each tile
@@ -358,8 +418,12 @@ __device__ __forceinline__ void merge_partitions(const DecodeParams& a, int s, i
     }
 }
 
+#ifndef PKV_MIN_CTAS_PER_SM
+#define PKV_MIN_CTAS_PER_SM 4
+#endif
+
 template <class E, int D, int BS>
-__global__ void __launch_bounds__(kThreads, 4) decode_kernel(DecodeParams a) {
+__global__ void __launch_bounds__(kThreads, PKV_MIN_CTAS_PER_SM) decode_kernel(DecodeParams a) {
     // wait for the plan kernel (programmatic dependent launch)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     __shared__ int s_item;
