@@ -403,7 +403,9 @@ def run_ours(args):
 
     if rank == 0:
         cfg = describe(w)
-        cfg.update({"partition_tokens": args.partition_tokens or 256,
+        chosen = int(st.workspace[8:12].view(torch.int32).item())  # plan kernel's choice
+        cfg.update({"partition_tokens": (f"auto ({chosen})" if not args.partition_tokens
+                                         else args.partition_tokens),
                     "l2": f"inputs larger than L2: {kv_bytes / 1e9:.2f} GB of KV read per step "
                           f"vs 129 MB L2; no flush",
                     "parallelism": f"replicas{world}" if world > 1 else "single GPU",

@@ -1,6 +1,10 @@
 // Cache maintenance kernels: slot mapping, the KV write of new tokens
 // (reshape_and_cache) and the copy-on-write block copy (copy_blocks).
 //
+// Each kernel is launched with programmatic dependent launch: it waits for
+// the kernel before it to finish (griddepcontrol.wait) before reading
+// anything, so only launch latency is overlapped, never data.
+//
 // All three move 16-byte vectors.  In the [NB][bs][H][D] layout a token's K
 // (or V) for all heads is one contiguous row of H*D elements and a block is
 // one contiguous run of bs*H*D elements, so both copies are plain streams of
@@ -17,6 +21,10 @@ __global__ void slot_mapping_kernel(int64_t* __restrict__ slot, const int32_t* _
                                     const int32_t* __restrict__ seq_idx,
                                     const int32_t* __restrict__ pos, int T, int S, int MB, int bs,
                                     int* err) {
+    // inputs may come from the kernel before this one; the next kernel may
+    // become resident once every CTA is past this point
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
     int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= T) return;
     int p = pos[t];
@@ -41,6 +49,10 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
     const uint4* __restrict__ key, const uint4* __restrict__ value, uint4* __restrict__ k_cache,
     uint4* __restrict__ v_cache, const int64_t* __restrict__ slot_mapping, int vec_per_row,
     int64_t num_slots, int* err) {
+    // inputs may come from the kernel before this one; the next kernel may
+    // become resident once every CTA is past this point
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
     const int t = blockIdx.x;
     const int64_t slot = slot_mapping[t];
     if (slot < 0) return;
@@ -65,6 +77,10 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
 __global__ void __launch_bounds__(256) copy_blocks_kernel(
     uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, const int64_t* __restrict__ mapping,
     int64_t vec_per_block, int NB, int* err) {
+    // inputs may come from the kernel before this one; the next kernel may
+    // become resident once every CTA is past this point
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
     const int p = blockIdx.x;
     const int64_t src = mapping[2 * p], dst = mapping[2 * p + 1];
     if (src < 0 || src >= NB || dst < 0 || dst >= NB) {
@@ -88,6 +104,21 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(
 
 bool supported(int D, int bs) { return (D == 64 || D == 128) && (bs == 16 || bs == 32); }
 
+template <class... KArgs, class... Args>
+cudaError_t launch_pdl(void (*fn)(KArgs...), dim3 grid, int threads, cudaStream_t st,
+                       Args... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(threads);
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fn, static_cast<KArgs>(args)...);
+}
+
 }  // namespace
 
 extern "C" {
@@ -102,9 +133,9 @@ pkv_status pkv_compute_slot_mapping(int64_t* slot_mapping, const int32_t* block_
     if (!slot_mapping || !seq_idx || !pos || (S > 0 && MB > 0 && !block_tables))
         return pkv::fail(PKV_ERR_INVALID_ARG, "compute_slot_mapping: null pointer");
     const int threads = 256;
-    slot_mapping_kernel<<<(T + threads - 1) / threads, threads, 0, pkv::as_stream(stream)>>>(
-        slot_mapping, block_tables, seq_idx, pos, T, S, MB, bs, pkv::device_error_word());
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(slot_mapping_kernel, dim3((T + threads - 1) / threads), threads,
+                               pkv::as_stream(stream), slot_mapping, block_tables, seq_idx, pos, T,
+                               S, MB, bs, pkv::device_error_word());
     return e == cudaSuccess ? PKV_OK : pkv::cuda_fail(e, "compute_slot_mapping launch");
 }
 
@@ -122,11 +153,11 @@ pkv_status pkv_reshape_and_cache(const void* key, const void* value, void* k_cac
         return pkv::fail(PKV_ERR_INVALID_ARG, "reshape_and_cache: pointers must be 16-byte aligned");
     const int vec_per_row = H * D / 8;
     const int threads = vec_per_row >= 256 ? 256 : ((vec_per_row + 31) / 32) * 32;
-    reshape_and_cache_kernel<<<T, threads, 0, pkv::as_stream(stream)>>>(
-        static_cast<const uint4*>(key), static_cast<const uint4*>(value), static_cast<uint4*>(k_cache),
-        static_cast<uint4*>(v_cache), slot_mapping, vec_per_row, (int64_t)NB * bs,
-        pkv::device_error_word());
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(reshape_and_cache_kernel, dim3(T), threads, pkv::as_stream(stream),
+                               static_cast<const uint4*>(key), static_cast<const uint4*>(value),
+                               static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+                               slot_mapping, vec_per_row, (int64_t)NB * bs,
+                               pkv::device_error_word());
     return e == cudaSuccess ? PKV_OK : pkv::cuda_fail(e, "reshape_and_cache launch");
 }
 
@@ -148,10 +179,9 @@ pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_ma
     if (splits > 64) splits = 64;
     if (splits < 1) splits = 1;
     dim3 grid(P, splits);
-    copy_blocks_kernel<<<grid, 256, 0, pkv::as_stream(stream)>>>(
-        static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), block_mapping, vec_per_block, NB,
-        pkv::device_error_word());
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(copy_blocks_kernel, grid, 256, pkv::as_stream(stream),
+                               static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+                               block_mapping, vec_per_block, NB, pkv::device_error_word());
     return e == cudaSuccess ? PKV_OK : pkv::cuda_fail(e, "copy_blocks launch");
 }
 

@@ -54,13 +54,16 @@ namespace {
 constexpr int kWarps = 4;                // heads per CTA, one warp per head
 constexpr int kThreads = 32 * kWarps;
 constexpr int kTile = 16;                // tokens per tile
-constexpr int kDefaultPartition = 256;   // tokens per split-K partition
-constexpr int kPlanThreads = 1024;
+constexpr int kMinAutoPartition = 64;    // smallest partition the automatic choice uses
+constexpr int kAutoCandidates = 7;       // 64, 128, ..., 4096 tokens
+constexpr int kItemsPerCta = 6;          // automatic choice: at least this many items per CTA
+constexpr int kPlanThreads = 256;
 constexpr unsigned kFull = 0xffffffffu;
 
 struct Workspace {
     unsigned* counter;  // next work item
     int* n_items;       // number of (sequence, partition) items
+    int* pt;            // tokens per partition chosen by the plan kernel
     int* items;         // packed (sequence << 16 | partition)
     int* nparts;        // partitions per sequence
     unsigned* tickets;  // per (sequence, head group): partitions finished
@@ -79,7 +82,7 @@ Layout layout_of(int S, int H, int D, int max_parts) {
     const size_t HG = (size_t)(H + kWarps - 1) / kWarps;
     const size_t part_elems = (size_t)S * H * max_parts;
     Layout L;
-    size_t o = 256;  // header: counter, n_items
+    size_t o = 256;  // header: counter, n_items, partition size
     L.items = o;   o = align256(o + (size_t)S * max_parts * sizeof(int));
     L.nparts = o;  o = align256(o + (size_t)S * sizeof(int));
     L.tickets = o; o = align256(o + (size_t)S * HG * sizeof(unsigned));
@@ -95,6 +98,7 @@ Workspace bind(void* base, const Layout& L) {
     Workspace w;
     w.counter = reinterpret_cast<unsigned*>(b);
     w.n_items = reinterpret_cast<int*>(b + 4);
+    w.pt = reinterpret_cast<int*>(b + 8);
     w.items = reinterpret_cast<int*>(b + L.items);
     w.nparts = reinterpret_cast<int*>(b + L.nparts);
     w.tickets = reinterpret_cast<unsigned*>(b + L.tickets);
@@ -111,7 +115,7 @@ struct DecodeParams {
     const void* v_cache;
     const int32_t* block_tables;
     const int32_t* context_lens;
-    int S, H, NB, MB, HG, PT, max_parts, max_ctx;
+    int S, H, NB, MB, HG, max_parts, max_ctx;
     float qscale;  // scale * log2(e)
     Workspace ws;
     int* err;
@@ -122,70 +126,124 @@ __device__ __forceinline__ int clamp_ctx(int c, int max_ctx) {
 }
 
 // ---------------------------------------------------------------------------
-// Plan: list the work items and reset the counter and the tickets.
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __restrict__ context_lens,
-                                                             int S, int PT, int max_ctx, int HG,
-                                                             Workspace ws, int* err) {
-    // the decode kernel may launch now; it waits for this grid to finish
+// Plan: choose the partition size, list the work items, reset the counter
+// and the tickets.  One CTA.
+//
+// Partition size when the caller leaves it to the library: the largest of
+// pt_min, 2*pt_min, ... that still gives every resident CTA at least
+// kItemsPerCta items (so the tail is short) and is at most half of the mean
+// context (so ragged contexts split into similar pieces).
+__global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const int32_t* __restrict__ context_lens,
+                                                                int S, int pt_fixed, int pt_min,
+                                                                int max_ctx, int slots, int HG,
+                                                                int n_tickets, Workspace ws, int* err) {
+    constexpr int kWarpsP = kPlanThreads / 32;
+    constexpr int kVals = 2 * kAutoCandidates + 1;  // full and all per candidate, sum of contexts
+    // context_lens may come from the kernel before this one
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the decode kernel may become resident now; it waits for this grid
     asm volatile("griddepcontrol.launch_dependents;");
-    __shared__ int warp_sum[2][32];
+    __shared__ int red[kWarpsP][kVals];
+    __shared__ int tot[kVals];
+    __shared__ int wsum[2][kWarpsP];
     __shared__ int carry[2];
-    __shared__ int n_full_total;
+    __shared__ int s_pt, s_full_total, s_items;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    for (int pass = 0; pass < 2; ++pass) {
-        if (tid == 0) carry[0] = carry[1] = 0;
-        __syncthreads();
-        for (int base = 0; base < S; base += kPlanThreads) {
-            const int s = base + tid;
-            int nf = 0, np = 0;
-            if (s < S) {
-                int c = context_lens[s];
-                if (c < 0 || c > max_ctx) {
-                    if (pass == 0) pkv::report(err, PKV_DEVERR_CONTEXT);
-                    c = clamp_ctx(c, max_ctx);
-                }
-                nf = c / PT;
-                np = (c % PT != 0 || c == 0) ? 1 : 0;  // an empty context still writes zeros
-            }
-            int a = nf, b = np;
+    const bool fixed = pt_fixed > 0;
+    const int ncand = fixed ? 1 : kAutoCandidates;
+
+    // per candidate partition size: full partitions and all partitions
+    int v[kVals];
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                int x = __shfl_up_sync(kFull, a, o), y = __shfl_up_sync(kFull, b, o);
-                if (lane >= o) { a += x; b += y; }
-            }
-            if (lane == 31) { warp_sum[0][wid] = a; warp_sum[1][wid] = b; }
-            __syncthreads();
-            if (wid == 0) {
-                int x = warp_sum[0][lane], y = warp_sum[1][lane];
-                int xi = x, yi = y;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    int u = __shfl_up_sync(kFull, xi, o), v = __shfl_up_sync(kFull, yi, o);
-                    if (lane >= o) { xi += u; yi += v; }
-                }
-                warp_sum[0][lane] = xi - x;  // exclusive
-                warp_sum[1][lane] = yi - y;
-            }
-            __syncthreads();
-            const int incl_f = a + warp_sum[0][wid], incl_p = b + warp_sum[1][wid];
-            if (pass == 1 && s < S) {
-                const int off_f = carry[0] + incl_f - nf, off_p = carry[1] + incl_p - np;
-                for (int k = 0; k < nf; ++k) ws.items[off_f + k] = (s << 16) | k;
-                if (np) ws.items[n_full_total + off_p] = (s << 16) | nf;
-                ws.nparts[s] = nf + np;
-            }
-            __syncthreads();
-            if (tid == kPlanThreads - 1) { carry[0] += incl_f; carry[1] += incl_p; }
-            __syncthreads();
+    for (int k = 0; k < kVals; ++k) v[k] = 0;
+    for (int s = tid; s < S; s += kPlanThreads) {
+        int c = context_lens[s];
+        if (c < 0 || c > max_ctx) {
+            pkv::report(err, PKV_DEVERR_CONTEXT);
+            c = clamp_ctx(c, max_ctx);
         }
-        if (pass == 0 && tid == 0) n_full_total = carry[0];
+        v[2 * kAutoCandidates] += c;
+#pragma unroll
+        for (int k = 0; k < kAutoCandidates; ++k) {
+            if (k < ncand) {
+                const int pt = fixed ? pt_fixed : (pt_min << k);
+                const int nf = c / pt;
+                v[k] += nf;
+                v[kAutoCandidates + k] += nf + ((c % pt != 0 || c == 0) ? 1 : 0);
+            }
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kVals; ++k) {
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) v[k] += __shfl_xor_sync(kFull, v[k], o);
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < kVals; ++k) red[wid][k] = v[k];
+    }
+    __syncthreads();
+    if (tid < kVals) {
+        int t = 0;
+#pragma unroll
+        for (int w = 0; w < kWarpsP; ++w) t += red[w][tid];
+        tot[tid] = t;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int pick = 0;
+        if (!fixed) {
+            const long long mean = S > 0 ? tot[2 * kAutoCandidates] / S : 0;
+            bool grow = true;
+#pragma unroll
+            for (int k = 1; k < kAutoCandidates; ++k) {
+                const long long cand = (long long)pt_min << k;
+                grow = grow && (long long)HG * tot[kAutoCandidates + k] >= (long long)kItemsPerCta * slots &&
+                       2 * cand <= mean;
+                if (grow) pick = k;
+            }
+        }
+        s_pt = fixed ? pt_fixed : (pt_min << pick);
+        s_full_total = tot[pick];
+        s_items = tot[kAutoCandidates + pick];
+        carry[0] = carry[1] = 0;
+    }
+    __syncthreads();
+    const int PT = s_pt;
+
+    // item list: full partitions first (sequence order), partial ones after
+    for (int base = 0; base < S; base += kPlanThreads) {
+        const int s = base + tid;
+        int nf = 0, np = 0;
+        if (s < S) {
+            const int c = clamp_ctx(context_lens[s], max_ctx);
+            nf = c / PT;
+            np = (c % PT != 0 || c == 0) ? 1 : 0;  // an empty context still writes zeros
+        }
+        int a = nf, b = np;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int x = __shfl_up_sync(kFull, a, o), y = __shfl_up_sync(kFull, b, o);
+            if (lane >= o) { a += x; b += y; }
+        }
+        if (lane == 31) { wsum[0][wid] = a; wsum[1][wid] = b; }
+        __syncthreads();
+        int off_f = carry[0] + a - nf, off_p = carry[1] + b - np;
+        for (int w = 0; w < wid; ++w) { off_f += wsum[0][w]; off_p += wsum[1][w]; }
+        if (s < S) {
+            for (int k = 0; k < nf; ++k) ws.items[off_f + k] = (s << 16) | k;
+            if (np) ws.items[s_full_total + off_p] = (s << 16) | nf;
+            ws.nparts[s] = nf + np;
+        }
+        __syncthreads();
+        if (tid == kPlanThreads - 1) { carry[0] = off_f + nf; carry[1] = off_p + np; }
         __syncthreads();
     }
-    for (int i = tid; i < S * HG; i += kPlanThreads) ws.tickets[i] = 0u;
+    for (int i = tid; i < n_tickets; i += kPlanThreads) ws.tickets[i] = 0u;
     if (tid == 0) {
         *ws.counter = 0u;
-        *ws.n_items = carry[0] + carry[1];
+        *ws.n_items = s_items;
+        *ws.pt = PT;
     }
 }
 
@@ -430,6 +488,7 @@ __global__ void __launch_bounds__(kThreads, PKV_MIN_CTAS_PER_SM) decode_kernel(D
     __shared__ int s_last;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int total = *a.ws.n_items * a.HG;
+    const int PT = *a.ws.pt;
     if (threadIdx.x == 0) s_item = (int)atomicAdd(a.ws.counter, 1u);
     __syncthreads();
     int item = s_item;
@@ -441,8 +500,8 @@ __global__ void __launch_bounds__(kThreads, PKV_MIN_CTAS_PER_SM) decode_kernel(D
         const int s = packed >> 16, part = packed & 0xffff;
         const int np = a.ws.nparts[s];
         const int ctx = clamp_ctx(a.context_lens[s], a.max_ctx);
-        const int t_begin = part * a.PT;
-        const int t_end = min(t_begin + a.PT, ctx);
+        const int t_begin = part * PT;
+        const int t_end = min(t_begin + PT, ctx);
         const int h = hg * kWarps + warp;
         if (h < a.H) attend_partition<E, D, BS>(a, s, h, part, t_begin, t_end, np, lane);
         if (np > 1) {
@@ -507,51 +566,85 @@ int max_parts_of(int max_ctx, int PT) {
     return mp < 1 ? 1 : mp;
 }
 
-}  // namespace
+// Partition sizing for one call.  A fixed partition_tokens is used as is;
+// 0 lets the plan kernel choose among pt_min, 2*pt_min, ... (see
+// plan_kernel), and the workspace is laid out for pt_min, the smallest.
+struct CallShape {
+    int pt_fixed;   // > 0: the caller's partition size; 0: automatic
+    int pt_min;     // smallest partition size the call may use
+    int max_ctx;
+    int max_parts;  // partitions of the longest context at pt_min
+    Layout L;
+};
 
-extern "C" {
-
-size_t pkv_decode_workspace_size(int S, int H, int D, int max_context_len, int partition_tokens) {
-    const int PT = partition_tokens == 0 ? kDefaultPartition : partition_tokens;
-    if (S < 0 || H <= 0 || (D != 64 && D != 128) || max_context_len < 0 || PT <= 0 || PT % kTile)
-        return 0;
-    return layout_of(S, H, D, max_parts_of(max_context_len, PT)).total;
+// Smallest automatic partition (64 * 2^k) whose layout fits `capacity`
+// bytes and gives at most 65535 partitions; 0 if none does.
+int auto_pt_min(int S, int H, int D, int max_ctx, size_t capacity) {
+    for (int k = 0; k < kAutoCandidates; ++k) {
+        const int pt = kMinAutoPartition << k;
+        const int mp = max_parts_of(max_ctx, pt);
+        if (mp <= 65535 && layout_of(S, H, D, mp).total <= capacity) return pt;
+    }
+    return 0;
 }
 
-pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_cache,
-                                      const void* v_cache, const int32_t* block_tables,
-                                      const int32_t* context_lens, int S, int H, int D, int bs,
-                                      int NB, int MB, int max_context_len, float scale,
-                                      pkv_dtype dtype, int partition_tokens, void* workspace,
-                                      size_t workspace_bytes, void* stream) {
-    pkv::clear_error();
+pkv_status check_call(const char* who, void* out, const void* q, const void* k_cache,
+                      const void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
+                      int S, int H, int D, int bs, int NB, int MB, int max_context_len,
+                      float scale, pkv_dtype dtype, int partition_tokens, size_t capacity,
+                      CallShape* cs) {
+    char msg[320];
+    auto bad = [&](pkv_status st, const char* what) {
+        snprintf(msg, sizeof msg, "%s: %s", who, what);
+        return pkv::fail(st, msg);
+    };
     if (S < 0 || H <= 0 || NB <= 0 || MB <= 0 || (dtype != PKV_F16 && dtype != PKV_BF16))
-        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode: bad size or dtype");
+        return bad(PKV_ERR_INVALID_ARG, "bad size or dtype");
     if ((D != 64 && D != 128) || (bs != 16 && bs != 32))
-        return pkv::fail(PKV_ERR_UNSUPPORTED, "paged_attention_decode: head_dim must be 64/128, block_size 16/32");
+        return bad(PKV_ERR_UNSUPPORTED, "head_dim must be 64/128, block_size 16/32");
     if (S == 0) return PKV_OK;
-    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace)
-        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode: null pointer");
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+        return bad(PKV_ERR_INVALID_ARG, "null pointer");
     if (!pkv::aligned16(out) || !pkv::aligned16(q) || !pkv::aligned16(k_cache) || !pkv::aligned16(v_cache))
-        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode: token pointers must be 16-byte aligned");
-    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode: workspace must be 256-byte aligned");
+        return bad(PKV_ERR_INVALID_ARG, "token pointers must be 16-byte aligned");
     const int64_t cap = (int64_t)MB * bs;
     const int max_ctx = max_context_len == 0 ? (int)(cap < INT32_MAX ? cap : INT32_MAX) : max_context_len;
-    if (max_ctx < 0 || max_ctx > cap)
-        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode: max_context_len must be in [0, MB*bs]");
-    const int PT = partition_tokens == 0 ? kDefaultPartition : partition_tokens;
-    if (PT <= 0 || PT % kTile != 0 || PT % bs != 0)
-        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode: partition_tokens must be a multiple of 16 and of block_size");
-    if (!(scale == scale) || std::isinf(scale))
-        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode: scale must be finite");
-    const int max_parts = max_parts_of(max_ctx, PT);
-    if (S > 32767 || max_parts > 65535)
-        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode: at most 32767 sequences and 65535 partitions");
-    const Layout L = layout_of(S, H, D, max_parts);
-    if (workspace_bytes < L.total)
-        return pkv::fail(PKV_ERR_WORKSPACE, "paged_attention_decode: workspace too small");
+    if (max_ctx < 0 || max_ctx > cap) return bad(PKV_ERR_INVALID_ARG, "max_context_len must be in [0, MB*bs]");
+    if (partition_tokens < 0 || (partition_tokens > 0 && (partition_tokens % kTile || partition_tokens % bs)))
+        return bad(PKV_ERR_INVALID_ARG, "partition_tokens must be 0 or a multiple of 16 and of block_size");
+    if (!(scale == scale) || std::isinf(scale)) return bad(PKV_ERR_INVALID_ARG, "scale must be finite");
+    if (S > 32767) return bad(PKV_ERR_INVALID_ARG, "at most 32767 sequences");
+    cs->max_ctx = max_ctx;
+    if (partition_tokens > 0) {
+        cs->pt_fixed = cs->pt_min = partition_tokens;
+    } else {
+        cs->pt_fixed = 0;
+        cs->pt_min = auto_pt_min(S, H, D, max_ctx, capacity);
+        if (cs->pt_min == 0) cs->pt_min = kMinAutoPartition << (kAutoCandidates - 1);
+    }
+    cs->max_parts = max_parts_of(max_ctx, cs->pt_min);
+    if (cs->max_parts > 65535 || (int64_t)S * cs->max_parts > INT32_MAX / 64)
+        return bad(PKV_ERR_INVALID_ARG, "too many partitions: raise partition_tokens");
+    cs->L = layout_of(S, H, D, cs->max_parts);
+    if (cs->L.total > capacity) {
+        snprintf(msg, sizeof msg, "%s: this size needs %zu bytes of workspace, %zu available", who,
+                 cs->L.total, capacity);
+        return pkv::fail(PKV_ERR_WORKSPACE, msg);
+    }
+    return PKV_OK;
+}
 
+cudaLaunchAttribute pdl_attr() {
+    cudaLaunchAttribute a;
+    a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a.val.programmaticStreamSerializationAllowed = 1;
+    return a;
+}
+
+pkv_status launch_decode(const char* who, const CallShape& cs, void* out, const void* q,
+                         const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                         const int32_t* context_lens, int S, int H, int D, int bs, int NB, int MB,
+                         float scale, pkv_dtype dtype, void* workspace, cudaStream_t st) {
     DecodeParams p;
     p.out = out;
     p.q = q;
@@ -564,36 +657,78 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_ca
     p.NB = NB;
     p.MB = MB;
     p.HG = (H + kWarps - 1) / kWarps;
-    p.PT = PT;
-    p.max_parts = max_parts;
-    p.max_ctx = max_ctx;
+    p.max_parts = cs.max_parts;
+    p.max_ctx = cs.max_ctx;
     p.qscale = scale * 1.4426950408889634f;  // log2(e)
-    p.ws = bind(workspace, L);
+    p.ws = bind(workspace, cs.L);
     p.err = pkv::device_error_word();
 
-    cudaStream_t st = pkv::as_stream(stream);
-    plan_kernel<<<1, kPlanThreads, 0, st>>>(context_lens, S, PT, max_ctx, p.HG, p.ws, p.err);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return pkv::cuda_fail(e, "paged_attention_decode plan launch");
-
     KernelFn fn = pick(dtype, D, bs);
-    const int64_t upper = (int64_t)S * max_parts * p.HG;
+    const int64_t upper = (int64_t)S * cs.max_parts * p.HG;
     const int64_t resident = (int64_t)resident_ctas(fn) * pkv::sm_count();
     const int grid = (int)(upper < resident ? upper : resident);
 
+    char msg[160];
+    cudaLaunchAttribute attr[1] = {pdl_attr()};
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(kPlanThreads);
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, plan_kernel, context_lens, S, cs.pt_fixed, cs.pt_min,
+                                       cs.max_ctx, grid, p.HG, S * H, p.ws, p.err);
+    if (e != cudaSuccess) {
+        snprintf(msg, sizeof msg, "%s plan launch", who);
+        return pkv::cuda_fail(e, msg);
+    }
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
     e = cudaLaunchKernelEx(&cfg, fn, p);
-    if (e != cudaSuccess) return pkv::cuda_fail(e, "paged_attention_decode launch");
+    if (e != cudaSuccess) {
+        snprintf(msg, sizeof msg, "%s launch", who);
+        return pkv::cuda_fail(e, msg);
+    }
     return PKV_OK;
+}
+}  // namespace
+
+extern "C" {
+
+size_t pkv_decode_workspace_size(int S, int H, int D, int max_context_len, int partition_tokens) {
+    if (S < 0 || H <= 0 || (D != 64 && D != 128) || max_context_len < 0 || partition_tokens < 0 ||
+        partition_tokens % kTile)
+        return 0;
+    int pt = partition_tokens;
+    if (pt == 0) pt = auto_pt_min(S, H, D, max_context_len, SIZE_MAX);
+    if (pt == 0) return 0;
+    const int mp = max_parts_of(max_context_len, pt);
+    if (mp > 65535) return 0;
+    return layout_of(S, H, D, mp).total;
+}
+
+pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_cache,
+                                      const void* v_cache, const int32_t* block_tables,
+                                      const int32_t* context_lens, int S, int H, int D, int bs,
+                                      int NB, int MB, int max_context_len, float scale,
+                                      pkv_dtype dtype, int partition_tokens, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+    static const char* who = "paged_attention_decode";
+    pkv::clear_error();
+    if (S > 0 && workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode: workspace must be 256-byte aligned");
+    CallShape cs;
+    // the automatic partition size is laid out for the smallest candidate,
+    // whatever the workspace holds: its size depends only on the arguments
+    pkv_status st = check_call(who, out, q, k_cache, v_cache, block_tables, context_lens, S, H, D,
+                               bs, NB, MB, max_context_len, scale, dtype, partition_tokens,
+                               SIZE_MAX, &cs);
+    if (st != PKV_OK || S == 0) return st;
+    if (!workspace) return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode: null workspace");
+    if (workspace_bytes < cs.L.total)
+        return pkv::fail(PKV_ERR_WORKSPACE, "paged_attention_decode: workspace too small");
+    return launch_decode(who, cs, out, q, k_cache, v_cache, block_tables, context_lens, S, H, D, bs,
+                         NB, MB, scale, dtype, workspace, pkv::as_stream(stream));
 }
 
 }  // extern "C"
@@ -643,84 +778,30 @@ extern "C" pkv_status pkv_paged_attention_decode_noalloc(
     const int32_t* block_tables, const int32_t* context_lens, int S, int H, int D, int bs, int NB,
     int MB, int max_context_len, float scale, pkv_dtype dtype, int partition_tokens,
     void* stream) {
+    static const char* who = "paged_attention_decode_noalloc";
     pkv::clear_error();
-    if (S < 0 || H <= 0 || NB <= 0 || MB <= 0 || (dtype != PKV_F16 && dtype != PKV_BF16))
-        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode_noalloc: bad size or dtype");
-    if ((D != 64 && D != 128) || (bs != 16 && bs != 32))
-        return pkv::fail(PKV_ERR_UNSUPPORTED, "paged_attention_decode_noalloc: head_dim must be 64/128, block_size 16/32");
-    if (S == 0) return PKV_OK;
-    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
-        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode_noalloc: null pointer");
-    if (!pkv::aligned16(out) || !pkv::aligned16(q) || !pkv::aligned16(k_cache) || !pkv::aligned16(v_cache))
-        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode_noalloc: token pointers must be 16-byte aligned");
-    const int64_t cap = (int64_t)MB * bs;
-    const int max_ctx = max_context_len == 0 ? (int)(cap < INT32_MAX ? cap : INT32_MAX) : max_context_len;
-    if (max_ctx < 0 || max_ctx > cap)
-        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode_noalloc: max_context_len must be in [0, MB*bs]");
-    const int PT = partition_tokens == 0 ? kDefaultPartition : partition_tokens;
-    if (PT <= 0 || PT % kTile != 0 || PT % bs != 0)
-        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode_noalloc: partition_tokens must be a multiple of 16 and of block_size");
-    if (!(scale == scale) || std::isinf(scale))
-        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode_noalloc: scale must be finite");
-    const int max_parts = max_parts_of(max_ctx, PT);
-    if (S > 32767 || max_parts > 65535)
-        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode_noalloc: at most 32767 sequences and 65535 partitions");
-    const Layout L = layout_of(S, H, D, max_parts);
-    if (L.total > (size_t)PKV_NOALLOC_SCRATCH_BYTES) {
-        char msg[256];
+    CallShape cs;
+    // an automatic partition size starts from the smallest one whose
+    // partials fit the built-in scratch
+    pkv_status st = check_call(who, out, q, k_cache, v_cache, block_tables, context_lens, S, H, D,
+                               bs, NB, MB, max_context_len, scale, dtype, partition_tokens,
+                               (size_t)PKV_NOALLOC_SCRATCH_BYTES, &cs);
+    if (st == PKV_ERR_WORKSPACE) {
+        char msg[320];
         snprintf(msg, sizeof msg,
-                 "paged_attention_decode_noalloc: this size needs %zu bytes of scratch, more than the "
-                 "%u built into the library; call pkv_paged_attention_decode with a workspace",
-                 L.total, (unsigned)PKV_NOALLOC_SCRATCH_BYTES);
+                 "%s: this size needs %zu bytes of scratch, more than the %u built into the "
+                 "library; call pkv_paged_attention_decode with a workspace",
+                 who, cs.L.total, (unsigned)PKV_NOALLOC_SCRATCH_BYTES);
         return pkv::fail(PKV_ERR_WORKSPACE, msg);
     }
+    if (st != PKV_OK || S == 0) return st;
     void* scratch = nullptr;
-    pkv_status st = noalloc_scratch(&scratch);
+    st = noalloc_scratch(&scratch);
     if (st != PKV_OK) return st;
-
-    DecodeParams p;
-    p.out = out;
-    p.q = q;
-    p.k_cache = k_cache;
-    p.v_cache = v_cache;
-    p.block_tables = block_tables;
-    p.context_lens = context_lens;
-    p.S = S;
-    p.H = H;
-    p.NB = NB;
-    p.MB = MB;
-    p.HG = (H + kWarps - 1) / kWarps;
-    p.PT = PT;
-    p.max_parts = max_parts;
-    p.max_ctx = max_ctx;
-    p.qscale = scale * 1.4426950408889634f;  // log2(e)
-    p.ws = bind(scratch, L);
-    p.err = pkv::device_error_word();
-
     // The plan kernel rewrites the work counter, the item list, the
     // partition counts and the merge tickets at the start of every call;
     // each partial is written before it is read, so the previous call's
     // contents never reach the output.
-    cudaStream_t cs = pkv::as_stream(stream);
-    plan_kernel<<<1, kPlanThreads, 0, cs>>>(context_lens, S, PT, max_ctx, p.HG, p.ws, p.err);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return pkv::cuda_fail(e, "paged_attention_decode_noalloc plan launch");
-
-    KernelFn fn = pick(dtype, D, bs);
-    const int64_t upper = (int64_t)S * max_parts * p.HG;
-    const int64_t resident = (int64_t)resident_ctas(fn) * pkv::sm_count();
-    const int grid = (int)(upper < resident ? upper : resident);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = cs;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, fn, p);
-    if (e != cudaSuccess) return pkv::cuda_fail(e, "paged_attention_decode_noalloc launch");
-    return PKV_OK;
+    return launch_decode(who, cs, out, q, k_cache, v_cache, block_tables, context_lens, S, H, D, bs,
+                         NB, MB, scale, dtype, scratch, pkv::as_stream(stream));
 }

@@ -106,3 +106,24 @@ def test_shared_prefix_cow_full():
 def test_long_context_full(bs):
     r = compare_step(W.long_context(bs=bs))
     print(f"long_context_bs{bs} max abs", r["max_abs"])
+
+
+def _chosen_partition(st):
+    # the plan kernel records its partition size in the workspace header
+    return int(st.workspace[8:12].view(torch.int32).item())
+
+
+def test_automatic_partition_size_on_full_workloads():
+    """The automatic choice (largest of 64, 128, ... tokens giving >= 6 items
+    per resident CTA and <= half the mean context) on GB300's 152 SMs picks
+    the sizes measured fastest for these workloads."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if sms != 152:
+        pytest.skip("expected sizes are for a 152-SM GB300")
+    for make, want in ((W.llama7b_batch64, 128), (W.continuous_batching_bf16, 256),
+                       (W.shared_prefix, 512), (lambda: W.long_context(bs=16), 512)):
+        w = make()
+        st = device_step(w, 0)
+        st.run()
+        torch.cuda.synchronize()
+        assert _chosen_partition(st) == want, (w.name, _chosen_partition(st))
