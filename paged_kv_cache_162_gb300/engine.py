@@ -185,3 +185,34 @@ class DecodeStep:
                                      dtype_code(self.dtype), self.partition_tokens, self.workspace,
                                      self.workspace.numel(), stream)
         return self.out
+
+
+class StepGraph:
+    """One decode step captured in a CUDA graph, optionally with the copies
+    of its inputs from pinned host memory and of its output back to it.
+
+    h2d: [(device_tensor, pinned_host_tensor), ...] copied in first;
+    d2h: [(pinned_host_tensor, device_tensor), ...] copied out last.
+    The step runs once eagerly before capture so that every per-device
+    set-up of the library happens outside the capture.  replay() enqueues
+    the whole step on the capture stream with one launch.
+    """
+
+    def __init__(self, step: DecodeStep, stream: torch.cuda.Stream, h2d=(), d2h=()):
+        self.step = step
+        self.stream = stream
+        with torch.cuda.stream(stream):
+            step.run()
+        stream.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=stream):
+            for dev, host in h2d:
+                dev.copy_(host, non_blocking=True)
+            step.run()
+            for host, dev in d2h:
+                host.copy_(dev, non_blocking=True)
+
+    def replay(self):
+        """Enqueue the captured step on its stream (not torch's current one)."""
+        with torch.cuda.stream(self.stream):
+            self.graph.replay()
