@@ -49,6 +49,8 @@ def parse_args(argv=None):
     p.add_argument("--partition-tokens", type=int, default=0)
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--measure", choices=["step", "swap_blocks"], default="step",
+                   help="swap_blocks: GPU <-> pinned-host block copy bandwidth instead")
     return p.parse_args(argv)
 
 
@@ -477,8 +479,57 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_swap(args):
+    """GPU <-> pinned-host block copies (CPU swap) at the LLaMA-7B layer shape:
+    2048 blocks of 16 tokens x 32 heads x 128 fp16 (128 KB of K and 128 KB
+    of V each) out to a host pool and back into other GPU blocks."""
+    import numpy as np
+    import torch
+    from paged_kv_cache_162_gb300 import _lib as L
+    from paged_kv_cache_162_gb300.engine import swap_blocks
+
+    torch.cuda.set_device(0)
+    bs, H, D, NBg, P = 16, 32, 128, 8192, 2048
+    rng = np.random.default_rng(1005)
+    gk = torch.randn(NBg, bs, H, D, device="cuda").half()
+    gv = torch.randn(NBg, bs, H, D, device="cuda").half()
+    hk = torch.empty(P, bs, H, D, dtype=torch.float16).pin_memory()
+    hv = torch.empty(P, bs, H, D, dtype=torch.float16).pin_memory()
+    src = rng.permutation(NBg)[:P]
+    out_pairs = torch.from_numpy(np.stack([src, np.arange(P)], 1)).cuda()
+    dst = rng.permutation(np.setdiff1d(np.arange(NBg), src))[:P]
+    in_pairs = torch.from_numpy(np.stack([np.arange(P), dst], 1)).cuda()
+    stream = torch.cuda.Stream()
+    nbytes = P * 2 * bs * H * D * 2
+    res = {}
+    for name, pairs, direction in (("swap_out", out_pairs, L.PKV_SWAP_OUT),
+                                   ("swap_in", in_pairs, L.PKV_SWAP_IN)):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                swap_blocks(gk, gv, hk, hv, pairs, direction, stream)
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(max(1, min(args.steps, 50)))]
+            for a, b in evs:
+                a.record(stream)
+                swap_blocks(gk, gv, hk, hv, pairs, direction, stream)
+                b.record(stream)
+        stream.synchronize()
+        ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)
+        res[name] = {"ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9}
+    L.pkv_sync_check(stream)
+    assert torch.equal(gk[dst[:4]], hk[:4].cuda()) and torch.equal(gk[src[:4]], gk[dst[:4]])
+    print(json.dumps({"metric": "swap_blocks GB/s (K+V block payload per direction)",
+                      "unit": "GB/s", "blocks": P, "bytes_per_call": nbytes,
+                      "config": {"block_size": bs, "heads": H, "head_dim": D, "dtype": "f16",
+                                 "gpu_pool_blocks": NBg, "host": "pinned (cudaHostAlloc)"},
+                      **res}), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.impl == "ours" and args.measure == "swap_blocks":
+        run_swap(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -186,6 +186,30 @@ pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_ma
                            int P, int H, int D, int bs, int NB, pkv_dtype dtype,
                            void* stream);
 
+/* Swap directions for pkv_swap_blocks. */
+#define PKV_SWAP_OUT 0 /* GPU cache -> host cache */
+#define PKV_SWAP_IN 1  /* host cache -> GPU cache */
+
+/* Block copies between the GPU caches and host caches (CPU swap, [P1]
+ * 3.3.3: the KV of a sequence's blocks is copied page by page to CPU-side
+ * blocks so the GPU blocks can be freed, and copied back into freshly
+ * allocated GPU blocks later).  For each of the P pairs (src, dst) of
+ * block_mapping ([P][2] int64, device memory): PKV_SWAP_OUT copies GPU
+ * block src of gpu_k / gpu_v to host block dst of host_k / host_v;
+ * PKV_SWAP_IN copies host block src to GPU block dst.
+ *   gpu_k, gpu_v    [NB_gpu][bs][H][D] dtype, device memory
+ *   host_k, host_v  [NB_host][bs][H][D] dtype, page-locked host memory the
+ *                   device can address (cudaHostAlloc / cudaMallocHost, or
+ *                   cudaHostRegister'ed); anything else is
+ *                   PKV_ERR_INVALID_ARG.  One kernel moves every block over
+ *                   the CPU-GPU link, no per-block copy call.
+ * No destination block may appear twice in one call.  Ids outside their pool
+ * are skipped and set PKV_DEVERR_BLOCK_ID. */
+pkv_status pkv_swap_blocks(void* gpu_k, void* gpu_v, void* host_k, void* host_v,
+                           const int64_t* block_mapping, int P, int H, int D, int bs,
+                           int NB_gpu, int NB_host, pkv_dtype dtype, int direction,
+                           void* stream);
+
 /* Waits for `stream`, then returns PKV_ERR_CUDA if any asynchronous CUDA
  * error is pending. */
 pkv_status pkv_sync_check(void* stream);

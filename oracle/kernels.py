@@ -30,6 +30,8 @@ def lib():
         L.oracle_reshape_and_cache.restype = None
         L.oracle_copy_blocks.argtypes = [_P, _P, _P] + [ctypes.c_int] * 4 + [_P]
         L.oracle_copy_blocks.restype = None
+        L.oracle_swap_blocks.argtypes = [_P] * 5 + [ctypes.c_int] * 4
+        L.oracle_swap_blocks.restype = None
         L.oracle_decode.argtypes = ([_P] * 6 + [ctypes.c_int] * 5 + [ctypes.c_double, ctypes.c_int]
                                     + [_P, _P, ctypes.c_int, ctypes.c_int])
         L.oracle_decode.restype = ctypes.c_int
@@ -81,6 +83,16 @@ def copy_blocks(k_cache, v_cache, pairs, row_of_block=None):
     rob = _c(row_of_block, np.int32)
     lib().oracle_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(pr), pr.shape[0], H, D, bs,
                              _ptr(rob))
+
+
+def swap_blocks(dst_k, dst_v, src_k, src_v, pairs):
+    """In place on dst_k/dst_v; pairs: [P, 2] (src block, dst block)."""
+    for a in (dst_k, dst_v, src_k, src_v):
+        assert a.flags.c_contiguous and a.dtype == np.uint16
+    _, bs, H, D = src_k.shape
+    pr = _c(np.asarray(pairs, dtype=np.int64).reshape(-1, 2), np.int64)
+    lib().oracle_swap_blocks(_ptr(dst_k), _ptr(dst_v), _ptr(src_k), _ptr(src_v), _ptr(pr),
+                             pr.shape[0], H, D, bs)
 
 
 def decode(q, k_cache, v_cache, block_tables, context_lens, scale, is_bf16,

@@ -109,6 +109,21 @@ void oracle_copy_blocks(uint16_t* k_cache, uint16_t* v_cache, const int64_t* pai
     }
 }
 
+/* Swap copies between two block pools ([P1] 3.3.3, CPU swap: a sequence's
+ * blocks are copied page by page to CPU-side blocks, and back later): for
+ * each (src, dst) pair, in order, K block src of the source pool is copied to
+ * K block dst of the destination pool, and V likewise. */
+void oracle_swap_blocks(uint16_t* dst_k, uint16_t* dst_v, const uint16_t* src_k,
+                        const uint16_t* src_v, const int64_t* pairs, int P, int H, int D,
+                        int block_size) {
+    int64_t block_elems = (int64_t)block_size * H * D;
+    for (int i = 0; i < P; ++i) {
+        int64_t src = pairs[2 * i], dst = pairs[2 * i + 1];
+        memcpy(dst_k + dst * block_elems, src_k + src * block_elems, (size_t)block_elems * 2);
+        memcpy(dst_v + dst * block_elems, src_v + src * block_elems, (size_t)block_elems * 2);
+    }
+}
+
 /* ---- single-query decode attention, by definition ---------------------- */
 
 typedef struct {

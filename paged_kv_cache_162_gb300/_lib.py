@@ -28,6 +28,8 @@ PKV_DEVERR_SLOT = 0x2
 PKV_DEVERR_CONTEXT = 0x4
 PKV_DEVERR_POSITION = 0x8
 PKV_NOALLOC_SCRATCH_BYTES = 16 << 20
+PKV_SWAP_OUT = 0
+PKV_SWAP_IN = 1
 
 _STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
                  3: "PKV_ERR_OOM", 4: "PKV_ERR_WORKSPACE", 5: "PKV_ERR_CUDA"}
@@ -61,6 +63,7 @@ SIGNATURES = {
     "pkv_compute_slot_mapping": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "pkv_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "pkv_copy_blocks": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "pkv_swap_blocks": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "pkv_sync_check": (_I, [_P]),
     "pkv_get_device_errors": (_I, [_P]),
     "pkv_alloc_create": (_I, [_I32, _P]),
@@ -176,6 +179,13 @@ def pkv_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, T, H, D, b
 def pkv_copy_blocks(k_cache, v_cache, block_mapping, P, H, D, bs, NB, dtype, stream=None) -> None:
     check(lib().pkv_copy_blocks(ptr(k_cache), ptr(v_cache), ptr(block_mapping), P, H, D, bs, NB,
                                 int(dtype), stream_handle(stream)), "copy_blocks")
+
+
+def pkv_swap_blocks(gpu_k, gpu_v, host_k, host_v, block_mapping, P, H, D, bs, NB_gpu, NB_host,
+                    dtype, direction, stream=None) -> None:
+    check(lib().pkv_swap_blocks(ptr(gpu_k), ptr(gpu_v), ptr(host_k), ptr(host_v),
+                                ptr(block_mapping), P, H, D, bs, NB_gpu, NB_host, int(dtype),
+                                int(direction), stream_handle(stream)), "swap_blocks")
 
 
 def pkv_sync_check(stream=None) -> None:

@@ -125,3 +125,21 @@ def plan_step(alloc: BlockAllocator, tables_pre: np.ndarray, nblocks_pre: np.nda
             pairs.append(pr)
     pairs = np.concatenate(pairs) if pairs else np.zeros((0, 2), dtype=np.int64)
     return tables, nb, pairs
+
+
+def plan_swap_out(gpu: BlockAllocator, host: BlockAllocator, table):
+    """CPU swap-out of one sequence ("3.3 页面级显存管理" 3.3.3): a host block
+    for each of its GPU blocks.  Returns (host_ids, pairs [P, 2] gpu->host).
+    After the copy, call gpu.decref(table) to release the GPU blocks."""
+    host_ids = host.alloc(len(table))
+    pairs = np.array(list(zip(table, host_ids)), dtype=np.int64).reshape(-1, 2)
+    return host_ids, pairs
+
+
+def plan_swap_in(gpu: BlockAllocator, host: BlockAllocator, host_ids):
+    """CPU swap-in: fresh GPU blocks for a swapped-out sequence.  Returns
+    (table, pairs [P, 2] host->gpu).  After the copy, call
+    host.decref(host_ids) to release the host blocks."""
+    table = gpu.alloc(len(host_ids))
+    pairs = np.array(list(zip(host_ids, table)), dtype=np.int64).reshape(-1, 2)
+    return table, pairs

@@ -1,5 +1,6 @@
 // Cache maintenance kernels: slot mapping, the KV write of new tokens
-// (reshape_and_cache) and the copy-on-write block copy (copy_blocks).
+// (reshape_and_cache), the copy-on-write block copy (copy_blocks) and the
+// GPU <-> host block copy of CPU swap (swap_blocks).
 //
 // Each kernel is launched with programmatic dependent launch: it waits for
 // the kernel before it to finish (griddepcontrol.wait) before reading
@@ -73,33 +74,53 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
 }
 
 // Grid (P, splits): CTA (p, y) copies the y-th 1/splits of pair p's K block
-// and V block.
+// and V block from the source pool to the destination pool (the same pool
+// for copy-on-write, the GPU and the host pool for swaps).
 __global__ void __launch_bounds__(256) copy_blocks_kernel(
-    uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, const int64_t* __restrict__ mapping,
-    int64_t vec_per_block, int NB, int* err) {
+    uint4* __restrict__ dst_k, uint4* __restrict__ dst_v, const uint4* __restrict__ src_k,
+    const uint4* __restrict__ src_v, const int64_t* __restrict__ mapping, int64_t vec_per_block,
+    int NB_src, int NB_dst, int* err) {
     // inputs may come from the kernel before this one; the next kernel may
     // become resident once every CTA is past this point
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
     const int p = blockIdx.x;
     const int64_t src = mapping[2 * p], dst = mapping[2 * p + 1];
-    if (src < 0 || src >= NB || dst < 0 || dst >= NB) {
+    if (src < 0 || src >= NB_src || dst < 0 || dst >= NB_dst) {
         if (threadIdx.x == 0 && blockIdx.y == 0) pkv::report(err, PKV_DEVERR_BLOCK_ID);
         return;
     }
     const int64_t per = (vec_per_block + gridDim.y - 1) / gridDim.y;
     const int64_t lo = blockIdx.y * per;
     const int64_t hi = lo + per < vec_per_block ? lo + per : vec_per_block;
-    const uint4* ks = k_cache + src * vec_per_block;
-    const uint4* vs = v_cache + src * vec_per_block;
-    uint4* kd = k_cache + dst * vec_per_block;
-    uint4* vd = v_cache + dst * vec_per_block;
+    const uint4* ks = src_k + src * vec_per_block;
+    const uint4* vs = src_v + src * vec_per_block;
+    uint4* kd = dst_k + dst * vec_per_block;
+    uint4* vd = dst_v + dst * vec_per_block;
     for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x) {
         uint4 a = ks[i];
         uint4 b = vs[i];
         kd[i] = a;
         vd[i] = b;
     }
+}
+
+int copy_splits(int64_t vec_per_block) {
+    // ~16 KB of K and 16 KB of V per CTA
+    int64_t splits = (vec_per_block + 1023) / 1024;
+    return (int)(splits < 1 ? 1 : (splits > 64 ? 64 : splits));
+}
+
+// Device address of a page-locked host buffer (nullptr if the device cannot
+// address it).
+void* device_view_of_host(void* p) {
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (attr.type != cudaMemoryTypeHost) return nullptr;
+    return attr.devicePointer;
 }
 
 bool supported(int D, int bs) { return (D == 64 || D == 128) && (bs == 16 || bs == 32); }
@@ -174,15 +195,42 @@ pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_ma
         return pkv::fail(PKV_ERR_INVALID_ARG, "copy_blocks: pointers must be 16-byte aligned");
     if (P > 65535 * 64) return pkv::fail(PKV_ERR_INVALID_ARG, "copy_blocks: too many pairs");
     const int64_t vec_per_block = (int64_t)bs * H * D / 8;
-    // ~2 KB of K and 2 KB of V per thread-row pass; 16 KB of each per CTA
-    int splits = (int)((vec_per_block + 1023) / 1024);
-    if (splits > 64) splits = 64;
-    if (splits < 1) splits = 1;
-    dim3 grid(P, splits);
+    dim3 grid(P, copy_splits(vec_per_block));
     cudaError_t e = launch_pdl(copy_blocks_kernel, grid, 256, pkv::as_stream(stream),
                                static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
-                               block_mapping, vec_per_block, NB, pkv::device_error_word());
+                               static_cast<const uint4*>(k_cache), static_cast<const uint4*>(v_cache),
+                               block_mapping, vec_per_block, NB, NB, pkv::device_error_word());
     return e == cudaSuccess ? PKV_OK : pkv::cuda_fail(e, "copy_blocks launch");
+}
+
+pkv_status pkv_swap_blocks(void* gpu_k, void* gpu_v, void* host_k, void* host_v,
+                           const int64_t* block_mapping, int P, int H, int D, int bs, int NB_gpu,
+                           int NB_host, pkv_dtype dtype, int direction, void* stream) {
+    pkv::clear_error();
+    if (P < 0 || H <= 0 || NB_gpu < 0 || NB_host < 0 || (dtype != PKV_F16 && dtype != PKV_BF16) ||
+        (direction != PKV_SWAP_OUT && direction != PKV_SWAP_IN))
+        return pkv::fail(PKV_ERR_INVALID_ARG, "swap_blocks: bad size, dtype or direction");
+    if (!supported(D, bs)) return pkv::fail(PKV_ERR_UNSUPPORTED, "swap_blocks: unsupported head_dim/block_size");
+    if (P == 0) return PKV_OK;
+    if (P > 65535 * 64) return pkv::fail(PKV_ERR_INVALID_ARG, "swap_blocks: too many pairs");
+    if (!gpu_k || !gpu_v || !host_k || !host_v || !block_mapping)
+        return pkv::fail(PKV_ERR_INVALID_ARG, "swap_blocks: null pointer");
+    if (!pkv::aligned16(gpu_k) || !pkv::aligned16(gpu_v) || !pkv::aligned16(host_k) || !pkv::aligned16(host_v))
+        return pkv::fail(PKV_ERR_INVALID_ARG, "swap_blocks: pointers must be 16-byte aligned");
+    void* dk = device_view_of_host(host_k);
+    void* dv = device_view_of_host(host_v);
+    if (!dk || !dv)
+        return pkv::fail(PKV_ERR_INVALID_ARG, "swap_blocks: host caches must be page-locked host memory the device can address");
+    const int64_t vec_per_block = (int64_t)bs * H * D / 8;
+    dim3 grid(P, copy_splits(vec_per_block));
+    uint4 *gk = static_cast<uint4*>(gpu_k), *gv = static_cast<uint4*>(gpu_v);
+    uint4 *hk = static_cast<uint4*>(dk), *hv = static_cast<uint4*>(dv);
+    const bool out = direction == PKV_SWAP_OUT;
+    cudaError_t e = launch_pdl(copy_blocks_kernel, grid, 256, pkv::as_stream(stream),
+                               out ? hk : gk, out ? hv : gv, out ? gk : hk, out ? gv : hv,
+                               block_mapping, vec_per_block, out ? NB_gpu : NB_host,
+                               out ? NB_host : NB_gpu, pkv::device_error_word());
+    return e == cudaSuccess ? PKV_OK : pkv::cuda_fail(e, "swap_blocks launch");
 }
 
 }  // extern "C"

@@ -86,6 +86,16 @@ def copy_blocks(k_cache, v_cache, block_mapping, stream=None):
                       dtype_code(k_cache.dtype), stream)
 
 
+def swap_blocks(gpu_k, gpu_v, host_k, host_v, block_mapping, direction, stream=None):
+    """GPU <-> pinned-host block copies (CPU swap).  block_mapping [P, 2]
+    int64 on the device: (gpu block, host block) pairs for swap-out,
+    (host block, gpu block) pairs for swap-in."""
+    NBg, bs, H, D = gpu_k.shape
+    P = block_mapping.shape[0]
+    L.pkv_swap_blocks(gpu_k, gpu_v, host_k, host_v, block_mapping, P, H, D, bs, NBg,
+                      host_k.shape[0], dtype_code(gpu_k.dtype), direction, stream)
+
+
 class DecodeStep:
     """Device-resident state of one decode step and the calls that run it.
 

@@ -387,3 +387,28 @@ def test_continuous_batching_step_allocations():
     assert a.num_free + len(held) == w.NB
     # at most one partial block per sequence
     assert np.all(nb == -(-w.context_lens // w.bs))
+
+
+def test_swap_blocks_round_trip_and_fancy_indexing():
+    """Swap-out then swap-in into other blocks ([P1] 3.3.3): every block
+    lands where numpy's fancy indexing puts it, nothing else changes."""
+    rng = np.random.default_rng(21)
+    H, D, bs, NBg, NBh = 2, 8, 16, 12, 6
+    gk = rng.integers(0, 1 << 15, (NBg, bs, H, D)).astype(np.uint16)
+    gv = rng.integers(0, 1 << 15, (NBg, bs, H, D)).astype(np.uint16)
+    hk = np.zeros((NBh, bs, H, D), np.uint16)
+    hv = np.zeros_like(hk)
+    out = [[3, 5], [7, 0], [11, 2]]              # gpu block -> host block
+    K.swap_blocks(hk, hv, gk, gv, out)
+    want_k, want_v = np.zeros_like(hk), np.zeros_like(hv)
+    src, dst = np.array(out).T
+    want_k[dst], want_v[dst] = gk[src], gv[src]
+    assert np.array_equal(hk, want_k) and np.array_equal(hv, want_v)
+    back = [[5, 1], [0, 4], [2, 9]]              # host block -> other gpu blocks
+    g2k, g2v = gk.copy(), gv.copy()
+    K.swap_blocks(g2k, g2v, hk, hv, back)
+    for (g0, h), (h2, g1) in zip(out, back):
+        assert h == h2
+        assert np.array_equal(g2k[g1], gk[g0]) and np.array_equal(g2v[g1], gv[g0])
+    untouched = [b for b in range(NBg) if b not in (1, 4, 9)]
+    assert np.array_equal(g2k[untouched], gk[untouched])
