@@ -47,6 +47,8 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="llama7b_batch64")
     p.add_argument("--partition-tokens", type=int, default=0)
+    p.add_argument("--block-size", type=int, default=0,
+                   help="llama7b_batch64 only: another block size (8, 16, 32, 64)")
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--measure", choices=["step", "swap_blocks"], default="step",
@@ -166,18 +168,23 @@ def weak_value(bytes_per_rank, world, step_ms):
 
 # ------------------------------------------------------------- workloads
 def describe(w):
-    ctx = w.context_lens
+    import numpy as np
+    ctx = w.context_lens.astype(np.int64)
+    blocks = -(-ctx // w.bs)
     return {"workload": w.name, "seqs": w.S, "heads": w.H, "head_dim": w.D, "block_size": w.bs,
             "pool_blocks": w.NB, "context_min": int(ctx.min()), "context_max": int(ctx.max()),
             "context_sum": int(ctx.sum()), "new_tokens": w.T,
-            "kv_bytes_per_step": w.kv_bytes()}
+            "kv_bytes_per_step": w.kv_bytes(),
+            # the block-size trade-off: table entries vs unfilled slots in last blocks
+            "table_entries": int(blocks.sum()),
+            "unfilled_slot_fraction": float((blocks * w.bs - ctx).sum() / (blocks * w.bs).sum())}
 
 
-def make_workload(name, rank):
+def make_workload(name, rank, block_size=0):
     import workloads as W
     seed_shift = 7919 * rank  # each rank its own batch
     if name == "llama7b_batch64":
-        return W.llama7b_batch64(seed=1001 + seed_shift)
+        return W.llama7b_batch64(seed=1001 + seed_shift, bs=block_size or 16)
     if name == "continuous_batching_bf16":
         return W.continuous_batching_bf16(seed=1002 + seed_shift)
     if name == "shared_prefix":
@@ -293,7 +300,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
-    w = make_workload(args.workload, rank)
+    w = make_workload(args.workload, rank, args.block_size)
     st = DecodeStep(dtype=w.dtype, S=w.S, H=w.H, D=w.D, bs=w.bs, NB=w.NB, MB=w.MB, scale=w.scale,
                     ctx_before=w.ctx_before, n_new=w.n_new, tables_pre=w.tables_pre,
                     nblocks_pre=w.nblocks_pre, initial_free=w.initial_free, blocks=w.blocks,

@@ -28,7 +28,7 @@
  *    at once, an error raised while a kernel runs surfaces on a later call
  *    or through pkv_sync_check().
  *  - Supported shapes: D (head_dim) in {64, 128}, bs (block size) in
- *    {16, 32}; anything else returns PKV_ERR_UNSUPPORTED.
+ *    {8, 16, 32, 64}; anything else returns PKV_ERR_UNSUPPORTED.
  *  - Out-of-range ids (a physical block outside [0, NB), a slot outside
  *    [0, NB*bs), a context longer than MB*bs) are never dereferenced: the
  *    kernel skips the access and records PKV_DEVERR_* in a device error word

@@ -123,7 +123,9 @@ void* device_view_of_host(void* p) {
     return attr.devicePointer;
 }
 
-bool supported(int D, int bs) { return (D == 64 || D == 128) && (bs == 16 || bs == 32); }
+bool supported(int D, int bs) {
+    return (D == 64 || D == 128) && (bs == 8 || bs == 16 || bs == 32 || bs == 64);
+}
 
 template <class... KArgs, class... Args>
 cudaError_t launch_pdl(void (*fn)(KArgs...), dim3 grid, int threads, cudaStream_t st,

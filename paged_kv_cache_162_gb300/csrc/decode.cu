@@ -289,16 +289,28 @@ __device__ __forceinline__ float dot8<pkv::BF16>(const uint4& q, const uint4& k,
 
 // Loads the lane's NI rows (r, r + RPI, ...) of a 16-token tile: rows at or
 // past `nvalid` are zero and not read.  A full tile takes no predicates.
-template <int NI, int RPI>
-__device__ __forceinline__ void load_tile(uint4 (&dst)[NI], const uint16_t* base, int64_t rstride,
-                                          int nvalid, int r) {
+// A tile covers TB = max(1, 16 / BS) blocks; base[b] points at row r of the
+// tile's part in block b, and the lane's i-th row lies in block
+// (RPI * i) / BS (BS is a multiple of RPI, so this does not depend on r).
+template <int NI, int RPI, int BS>
+__device__ __forceinline__ void load_tile(uint4 (&dst)[NI], const uint16_t* const (&base)[(BS < kTile) ? kTile / BS : 1],
+                                          int64_t HD, int nvalid, int r) {
+    constexpr int TB = (BS < kTile) ? kTile / BS : 1;
+    constexpr int SPAN = (BS < kTile) ? BS : kTile;  // tile rows per block
     if (nvalid == kTile) {
 #pragma unroll
-        for (int i = 0; i < NI; ++i) dst[i] = pkv::ld_stream(base + i * rstride);
+        for (int i = 0; i < NI; ++i) {
+            const int b = (RPI * i) / SPAN;
+            dst[i] = pkv::ld_stream(base[b < TB ? b : 0] + (RPI * i - b * SPAN) * HD);
+        }
     } else {
 #pragma unroll
-        for (int i = 0; i < NI; ++i)
-            dst[i] = (RPI * i + r < nvalid) ? pkv::ld_stream(base + i * rstride) : make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < NI; ++i) {
+            const int b = (RPI * i) / SPAN;
+            dst[i] = (RPI * i + r < nvalid)
+                         ? pkv::ld_stream(base[b < TB ? b : 0] + (RPI * i - b * SPAN) * HD)
+                         : make_uint4(0, 0, 0, 0);
+        }
     }
 }
 
@@ -310,7 +322,6 @@ __device__ __forceinline__ void attend_partition(const DecodeParams& a, int s, i
     constexpr int NI = kTile / RPI;    // warp-wide loads per tile (K and V each)
     const int r = lane / LPR, c = lane % LPR;
     const int64_t HD = (int64_t)a.H * D;
-    const int64_t rstride = RPI * HD;  // elements between a lane's rows
 
     const uint4 qv = __ldg(reinterpret_cast<const uint4*>(
         static_cast<const uint16_t*>(a.q) + ((int64_t)s * a.H + h) * D + c * 8));
@@ -324,15 +335,32 @@ __device__ __forceinline__ void attend_partition(const DecodeParams& a, int s, i
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j] = 0.f;
 
-    // valid rows of the tile at t0 (0 if its block id is out of range) and
-    // its element offset in the cache
-    auto locate = [&](int t0, int& nvalid) -> int64_t {
-        const int lb = t0 / BS;
-        const int phys = __ldg(bt_row + lb);
-        const bool ok = (unsigned)phys < (unsigned)a.NB;
-        if (!ok && lane == 0) pkv::report(a.err, PKV_DEVERR_BLOCK_ID);
-        nvalid = ok ? min(kTile, t_end - t0) : 0;
-        return ((int64_t)(ok ? phys : 0) * BS + (t0 - lb * BS)) * HD;
+    constexpr int TB = (BS < kTile) ? kTile / BS : 1;  // blocks per tile
+    // element offsets of the tile at t0 in each of its TB blocks, and its
+    // valid rows (masked from the first block whose id is out of range)
+    auto locate = [&](int t0, int64_t (&off)[TB], int& nvalid) {
+        nvalid = min(kTile, t_end - t0);
+#pragma unroll
+        for (int b = 0; b < TB; ++b) {
+            const int tb = t0 + b * BS;  // first token of this block's part
+            int phys = 0;
+            if (tb < t_end) {
+                const int lb = tb / BS;
+                phys = __ldg(bt_row + lb);
+                if ((unsigned)phys >= (unsigned)a.NB) {
+                    if (lane == 0) pkv::report(a.err, PKV_DEVERR_BLOCK_ID);
+                    nvalid = min(nvalid, b * BS);
+                    phys = 0;
+                }
+                off[b] = ((int64_t)phys * BS + (tb - lb * BS)) * HD;
+            } else {
+                off[b] = 0;
+            }
+        }
+    };
+    auto bases = [&](const uint16_t* p, const int64_t (&off)[TB], const uint16_t* (&out)[TB]) {
+#pragma unroll
+        for (int b = 0; b < TB; ++b) out[b] = p + off[b];
     };
 
     if (t_begin < t_end) {
@@ -340,20 +368,28 @@ __device__ __forceinline__ void attend_partition(const DecodeParams& a, int s, i
         // loads fly while P.V(t) is accumulated
         uint4 kr[NI], vr[NI];
         int nv;
-        int64_t off = locate(t_begin, nv);
-        load_tile<NI, RPI>(kr, kb + off, rstride, nv, r);
-        load_tile<NI, RPI>(vr, vb + off, rstride, nv, r);
+        int64_t off[TB];
+        const uint16_t* pb[TB];
+        locate(t_begin, off, nv);
+        bases(kb, off, pb);
+        load_tile<NI, RPI, BS>(kr, pb, HD, nv, r);
+        bases(vb, off, pb);
+        load_tile<NI, RPI, BS>(vr, pb, HD, nv, r);
         for (int t0 = t_begin;;) {
             const int t1 = t0 + kTile;
             const bool more = t1 < t_end;
             int nv1 = 0;
-            const int64_t off1 = more ? locate(t1, nv1) : 0;
+            int64_t off1[TB];
+            if (more) locate(t1, off1, nv1);
 
             // partial dots over this lane's 8 dims, one per loaded row
             float pd[NI];
 #pragma unroll
             for (int i = 0; i < NI; ++i) pd[i] = dot8<E>(qv, kr[i], 0.f);
-            if (more) load_tile<NI, RPI>(kr, kb + off1, rstride, nv1, r);
+            if (more) {
+                bases(kb, off1, pb);
+                load_tile<NI, RPI, BS>(kr, pb, HD, nv1, r);
+            }
             // reduce-scatter across the LPR lanes of a row group: after the
             // halving steps lane c holds row index c>>1 summed over half the
             // lanes, the xor-1 step completes the sum
@@ -391,7 +427,8 @@ __device__ __forceinline__ void attend_partition(const DecodeParams& a, int s, i
             }
             m_run = m_new;
             if (!more) break;
-            load_tile<NI, RPI>(vr, vb + off1, rstride, nv1, r);
+            bases(vb, off1, pb);
+            load_tile<NI, RPI, BS>(vr, pb, HD, nv1, r);
             t0 = t1;
             nv = nv1;
         }
@@ -531,7 +568,12 @@ using KernelFn = void (*)(DecodeParams);
 
 template <class E, int D>
 KernelFn pick_bs(int bs) {
-    return bs == 16 ? decode_kernel<E, D, 16> : decode_kernel<E, D, 32>;
+    switch (bs) {
+        case 8: return decode_kernel<E, D, 8>;
+        case 16: return decode_kernel<E, D, 16>;
+        case 32: return decode_kernel<E, D, 32>;
+        default: return decode_kernel<E, D, 64>;
+    }
 }
 
 template <class E>
@@ -600,8 +642,8 @@ pkv_status check_call(const char* who, void* out, const void* q, const void* k_c
     };
     if (S < 0 || H <= 0 || NB <= 0 || MB <= 0 || (dtype != PKV_F16 && dtype != PKV_BF16))
         return bad(PKV_ERR_INVALID_ARG, "bad size or dtype");
-    if ((D != 64 && D != 128) || (bs != 16 && bs != 32))
-        return bad(PKV_ERR_UNSUPPORTED, "head_dim must be 64/128, block_size 16/32");
+    if ((D != 64 && D != 128) || (bs != 8 && bs != 16 && bs != 32 && bs != 64))
+        return bad(PKV_ERR_UNSUPPORTED, "head_dim must be 64/128, block_size 8/16/32/64");
     if (S == 0) return PKV_OK;
     if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
         return bad(PKV_ERR_INVALID_ARG, "null pointer");

@@ -57,7 +57,7 @@ def _decode_args(**kw):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(D=96), L.PKV_ERR_UNSUPPORTED),
-    (dict(bs=8), L.PKV_ERR_UNSUPPORTED),
+    (dict(bs=24), L.PKV_ERR_UNSUPPORTED),
     (dict(dtype=7), L.PKV_ERR_INVALID_ARG),
     (dict(q=0), L.PKV_ERR_INVALID_ARG),
     (dict(out=18), L.PKV_ERR_INVALID_ARG),          # misaligned

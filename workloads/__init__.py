@@ -241,11 +241,13 @@ def tiny(seed=1000) -> Workload:
                           NB=64, MB=7)
 
 
-def llama7b_batch64(seed=1001, S=64) -> Workload:
+def llama7b_batch64(seed=1001, S=64, bs=16) -> Workload:
     """LLaMA-7B-shaped layer: 64 seqs, 32 x 128, fp16, bs 16, ctx U{128..2048},
-    pool = total need + 10 %, shuffled placement; one new token per seq."""
-    return uniform_decode("llama7b_batch64", seed, F16, S=S, H=32, D=128, bs=16,
-                          ctx_lo=128, ctx_hi=2048, MB=128)
+    pool = total need + 10 %, shuffled placement; one new token per seq.
+    `bs` changes only the block size (the block-size sweep)."""
+    return uniform_decode("llama7b_batch64" if bs == 16 else f"llama7b_batch64_bs{bs}", seed, F16,
+                          S=S, H=32, D=128, bs=bs, ctx_lo=128, ctx_hi=2048,
+                          MB=-(-2048 // bs))
 
 
 def long_context(bs=16, seed=1004, S=8, ctx_len=32768, NB=40000) -> Workload:
