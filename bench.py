@@ -51,8 +51,9 @@ def parse_args(argv=None):
                    help="llama7b_batch64 only: another block size (8, 16, 32, 64)")
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--measure", choices=["step", "swap_blocks"], default="step",
-                   help="swap_blocks: GPU <-> pinned-host block copy bandwidth instead")
+    p.add_argument("--measure", choices=["step", "swap_blocks", "beam_search"], default="step",
+                   help="swap_blocks: GPU <-> pinned-host block copies; beam_search: fork + "
+                        "copy-on-write every step")
     return p.parse_args(argv)
 
 
@@ -532,10 +533,64 @@ def run_swap(args):
                       **res}), flush=True)
 
 
+def run_beam(args):
+    """Beam search at scale: 16 requests x 4 beams at the LLaMA-7B layer shape,
+    every step a fork of all 64 sequences (shared tables), copy-on-write of
+    the shared partial blocks, the cache write and decode.  Times whole steps
+    (host allocator work, uploads, kernels, sync) and the host part alone."""
+    import numpy as np
+    import torch
+    import workloads as W
+    from paged_kv_cache_162_gb300 import _lib as L
+    from paged_kv_cache_162_gb300.engine import DecodeStep
+
+    torch.cuda.set_device(0)
+    steps = 64
+    bw = W.beam_search(steps=steps)
+    w = bw.init
+    st = DecodeStep(dtype=w.dtype, S=w.S, H=w.H, D=w.D, bs=w.bs, NB=w.NB, MB=w.MB, scale=w.scale,
+                    ctx_before=w.ctx_before, n_new=w.n_new, tables_pre=w.tables_pre,
+                    nblocks_pre=w.nblocks_pre, initial_free=w.initial_free, blocks=w.blocks,
+                    k_blocks=w.k_blocks, v_blocks=w.v_blocks, q=w.q, new_k=w.new_k,
+                    new_v=w.new_v, seq_idx=w.seq_idx, pos=w.pos,
+                    fill_bits=int(W.POISON[w.dtype]))
+    st.plan()
+    wall, host, pairs, kv, alloc_s = [], [], [], [], []
+    for i in range(steps):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        p = st.beam_step(bw.parents[i], bw.new_k[i], bw.new_v[i], bw.q[i])
+        t1 = time.perf_counter()
+        torch.cuda.synchronize()
+        t2 = time.perf_counter()
+        wall.append(t2 - t0)
+        host.append(t1 - t0)
+        alloc_s.append(st.last_allocator_seconds)
+        pairs.append(len(p))
+        kv.append(int(st.context_lens_host.astype(np.int64).sum()) * w.H * w.D * 4)
+    L.pkv_sync_check()
+    assert L.pkv_get_device_errors() == 0
+    warm = slice(4, None)
+    wall_ms = 1e3 * float(np.mean(wall[warm]))
+    print(json.dumps({
+        "metric": "beam-search steps/s (fork + copy-on-write + cache write + decode, 64 beams)",
+        "unit": "steps/s", "value": 1e3 / wall_ms, "ms_per_step": wall_ms,
+        "host_ms_per_step": 1e3 * float(np.mean(host[warm])),
+        "allocator_us_per_step": 1e6 * float(np.mean(alloc_s[warm])),
+        "copy_pairs_per_step": float(np.mean(pairs[warm])),
+        "logical_kv_gbs": float(np.mean(kv[warm])) / (wall_ms * 1e-3) / 1e9,
+        "config": {"requests": 16, "beams": 4, "heads": w.H, "head_dim": w.D,
+                   "block_size": w.bs, "prompt_tokens": "U{256..1024}", "steps": steps,
+                   "timed_steps": steps - 4}}), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "ours" and args.measure == "swap_blocks":
         run_swap(args)
+        return
+    if args.impl == "ours" and args.measure == "beam_search":
+        run_beam(args)
         return
     if args.impl == "reference":
         run_reference(args)

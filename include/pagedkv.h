@@ -277,6 +277,29 @@ pkv_status pkv_alloc_append(pkv_allocator* a, int32_t* table, int32_t* num_block
                             int32_t max_blocks, int32_t ctx_before, int32_t n_new,
                             int32_t bs, int64_t* pairs, int32_t* n_pairs);
 
+/* Batched append for S sequences whose tables are the rows of tables
+ * ([S][MB] int32, row s has num_blocks[s] valid entries): for s = 0, 1, ...
+ * in order, the same as pkv_alloc_append(row s, ctx_before[s], n_new[s]).
+ * Copy pairs of all sequences go to pairs[2*k], pairs[2*k+1] (room for
+ * max_pairs pairs; sequence s is only started if n_new[s]/bs + 2 more pairs
+ * fit); *n_pairs receives their number.  On PKV_ERR_OOM (or a full pairs
+ * buffer, PKV_ERR_INVALID_ARG) sequences [0, *n_done) have been extended and
+ * the rest are untouched; *n_done = S on success. */
+pkv_status pkv_alloc_append_batch(pkv_allocator* a, int32_t* tables, int32_t* num_blocks,
+                                  int32_t S, int32_t MB, const int32_t* ctx_before,
+                                  const int32_t* n_new, int32_t bs, int64_t* pairs,
+                                  int32_t max_pairs, int32_t* n_pairs, int32_t* n_done);
+
+/* Fork (beam search, parallel sampling: [P1] 3.3.2 share_blocks; [P4]
+ * "Memory Sharing与写时复制"): row s of tables ([S][MB] int32, num_blocks[s]
+ * entries) becomes a copy of row parents[s] of the old tables.  A hold is
+ * taken on every block of the new rows before the holds of the old rows are
+ * released, so a block that survives the fork never reaches refcount 0.
+ * All-or-nothing: an invalid parent, an entry that is not a held block or a
+ * release that would underflow changes nothing (PKV_ERR_INVALID_ARG). */
+pkv_status pkv_alloc_fork(pkv_allocator* a, int32_t* tables, int32_t* num_blocks, int32_t S,
+                          int32_t MB, const int32_t* parents);
+
 /* Reference count of block id (0 = free). */
 pkv_status pkv_alloc_refcount(const pkv_allocator* a, int32_t id, int32_t* rc);
 

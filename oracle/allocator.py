@@ -144,3 +144,17 @@ class BlockAllocatorModel:
             table[lb] = new
         table.extend(self.alloc(need_new))
         return pairs
+
+
+def fork_tables(alloc: BlockAllocatorModel, tables: list, parents) -> list:
+    """Every sequence b continues from sequence parents[b]: it takes a new
+    hold on each of the parent's blocks ([P1] 3.3.2 share_blocks; beam search
+    and parallel sampling in [P4] "Memory Sharing与写时复制"), then the old
+    tables are released.  Taking the new holds first keeps blocks that
+    survive the fork from passing through refcount 0."""
+    new = [list(tables[int(p)]) for p in parents]
+    for t in new:
+        alloc.incref(t)
+    for t in tables:
+        alloc.decref(t)
+    return new

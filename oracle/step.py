@@ -19,7 +19,7 @@ from dataclasses import dataclass
 import numpy as np
 
 from . import kernels
-from .allocator import BlockAllocatorModel
+from .allocator import BlockAllocatorModel, fork_tables
 
 
 @dataclass
@@ -96,3 +96,42 @@ def run(w, items=None, nthreads=None, keep_pre=False, attention=True) -> OracleS
     return OracleStep(tables=tables, nblocks=nb, pairs=pairs, slots=slots, pool_ids=ids,
                       row_of_block=rob, k_pool=k_pool, v_pool=v_pool, out=out, allocator=a,
                       k_pre=k_pre, v_pre=v_pre)
+
+
+def run_beam(bw, nthreads=None, items=None):
+    """Beam search by the oracle: yields, after each step, (tables [S, MB],
+    pairs [P, 2], slots [S], k_pool, v_pool, pool_ids, out [S, H, D])."""
+    from workloads import POISON, BF16
+    w = bw.init
+    if nthreads is None:
+        nthreads = kernels.default_threads()
+    a = rebuild_allocator(w)
+    tables = [w.tables_pre[s, :w.nblocks_pre[s]].tolist() for s in range(w.S)]
+    ctx = w.ctx_before.astype(np.int64).copy()
+    # every block the run can touch lives in the compact pool from the start
+    ids = np.arange(w.NB, dtype=np.int32)
+    rob = ids.copy()
+    k_pool = np.full((w.NB, w.bs, w.H, w.D), POISON[w.dtype], dtype=np.uint16)
+    v_pool = k_pool.copy()
+    if len(w.blocks):
+        k_pool[w.blocks], v_pool[w.blocks] = w.k_blocks, w.v_blocks
+    for i in range(bw.steps):
+        parents = bw.parents[i]
+        tables = fork_tables(a, tables, parents)
+        ctx = ctx[parents]
+        pairs = []
+        for b in range(w.S):
+            pairs += a.append(tables[b], int(ctx[b]), 1, w.bs)
+        pairs = np.array(pairs, dtype=np.int64).reshape(-1, 2)
+        bt = np.full((w.S, w.MB), -1, dtype=np.int32)
+        for b, t in enumerate(tables):
+            bt[b, :len(t)] = t
+        kernels.copy_blocks(k_pool, v_pool, pairs, row_of_block=rob)
+        seq_idx = np.arange(w.S, dtype=np.int32)
+        slots = kernels.slot_mapping(bt, seq_idx, ctx.astype(np.int32), w.bs)
+        kernels.reshape_and_cache(k_pool, v_pool, bw.new_k[i], bw.new_v[i], slots,
+                                  row_of_block=rob)
+        ctx = ctx + 1
+        out = kernels.decode(bw.q[i], k_pool, v_pool, bt, ctx.astype(np.int32), w.scale,
+                             w.dtype == BF16, row_of_block=rob, items=items, nthreads=nthreads)
+        yield bt, pairs, slots, k_pool, v_pool, ids, out

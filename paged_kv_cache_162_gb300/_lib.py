@@ -74,6 +74,8 @@ SIGNATURES = {
     "pkv_alloc_decref": (_I, [_P, _P, _I32, _P]),
     "pkv_alloc_cow": (_I, [_P, _I32, _P, _P]),
     "pkv_alloc_append": (_I, [_P, _P, _P, _I32, _I32, _I32, _I32, _P, _P]),
+    "pkv_alloc_append_batch": (_I, [_P, _P, _P, _I32, _I32, _P, _P, _I32, _P, _I32, _P, _P]),
+    "pkv_alloc_fork": (_I, [_P, _P, _P, _I32, _I32, _P]),
     "pkv_alloc_refcount": (_I, [_P, _I32, _P]),
     "pkv_alloc_num_blocks": (_I32, [_P]),
     "pkv_alloc_num_free": (_I32, [_P]),

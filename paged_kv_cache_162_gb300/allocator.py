@@ -88,6 +88,35 @@ class BlockAllocator:
         table[:] = row[:nb].tolist()
         return [tuple(int(x) for x in p) for p in pairs]
 
+    def append_batch(self, tables: np.ndarray, nblocks: np.ndarray, ctx_before, n_new,
+                     block_size: int):
+        """append() for every row of `tables` ([S, MB] int32, in place; nblocks
+        [S] int32 in place) in one native call.  Returns the copy pairs
+        [P, 2]; raises OutOfBlocks (rows before the failing one are done)."""
+        assert tables.dtype == np.int32 and tables.flags.c_contiguous
+        assert nblocks.dtype == np.int32 and nblocks.flags.c_contiguous
+        S, MB = tables.shape
+        cb = _i32(ctx_before)
+        nn = _i32(n_new)
+        cap = int((nn.astype(np.int64) // int(block_size) + 2).sum())
+        pairs = np.empty(2 * max(cap, 1), dtype=np.int64)
+        npairs, ndone = ctypes.c_int32(0), ctypes.c_int32(0)
+        check(lib().pkv_alloc_append_batch(self._h, tables.ctypes.data, nblocks.ctypes.data, S, MB,
+                                           cb.ctypes.data, nn.ctypes.data, int(block_size),
+                                           pairs.ctypes.data, cap, ctypes.addressof(npairs),
+                                           ctypes.addressof(ndone)), "alloc_append_batch")
+        return pairs[:2 * npairs.value].reshape(-1, 2)
+
+    def fork(self, tables: np.ndarray, nblocks: np.ndarray, parents) -> None:
+        """Row s becomes a copy of row parents[s] (in place), sharing its
+        blocks; one native call, all-or-nothing."""
+        assert tables.dtype == np.int32 and tables.flags.c_contiguous
+        assert nblocks.dtype == np.int32 and nblocks.flags.c_contiguous
+        S, MB = tables.shape
+        par = _i32(parents)
+        check(lib().pkv_alloc_fork(self._h, tables.ctypes.data, nblocks.ctypes.data, S, MB,
+                                   par.ctypes.data), "alloc_fork")
+
     def refcount(self, block: int) -> int:
         rc = ctypes.c_int32(0)
         check(lib().pkv_alloc_refcount(self._h, int(block), ctypes.addressof(rc)),
@@ -114,16 +143,9 @@ def plan_step(alloc: BlockAllocator, tables_pre: np.ndarray, nblocks_pre: np.nda
 
     Returns (tables [S, MB] int32, nblocks [S] int32, pairs [P, 2] int64).
     """
-    tables = np.array(tables_pre, dtype=np.int32, copy=True)
+    tables = np.array(tables_pre, dtype=np.int32, copy=True, order="C")
     nb = np.array(nblocks_pre, dtype=np.int32, copy=True)
-    pairs = []
-    for s in range(tables.shape[0]):
-        row = tables[s]
-        nb[s], pr = alloc.append_row(row, int(nb[s]), int(ctx_before[s]), int(n_new[s]),
-                                     block_size)
-        if len(pr):
-            pairs.append(pr)
-    pairs = np.concatenate(pairs) if pairs else np.zeros((0, 2), dtype=np.int64)
+    pairs = alloc.append_batch(tables, nb, ctx_before, n_new, block_size)
     return tables, nb, pairs
 
 
@@ -143,3 +165,20 @@ def plan_swap_in(gpu: BlockAllocator, host: BlockAllocator, host_ids):
     table = gpu.alloc(len(host_ids))
     pairs = np.array(list(zip(host_ids, table)), dtype=np.int64).reshape(-1, 2)
     return table, pairs
+
+
+def fork_tables(alloc: BlockAllocator, tables: list, parents) -> list:
+    """Beam-search / parallel-sampling fork: sequence b continues from
+    sequence parents[b].  Each new table takes a hold on every block of its
+    parent's table (sharing, "3.3 页面级显存管理" 3.3.2), then the old tables
+    are released, so blocks that survive the fork never reach refcount 0.
+    The next write into a block shared this way is copied first
+    (copy-on-write, by `append`)."""
+    new = [list(tables[int(p)]) for p in parents]
+    ids = [b for t in new for b in t]
+    if ids:
+        alloc.incref(ids)
+    old = [b for t in tables for b in t]
+    if old:
+        alloc.decref(old)
+    return new

@@ -12,6 +12,7 @@
 // Layout: `stack` holds the free ids (top = stack[top-1]) and `rc` the
 // count of every block (0 = free).  Every operation validates all of its
 // inputs before changing anything, so a failure leaves the pool as it was.
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <new>
@@ -196,6 +197,97 @@ pkv_status pkv_alloc_append(pkv_allocator* a, int32_t* table, int32_t* num_block
     for (int64_t i = 0; i < fresh; ++i) table[nb + i] = pop(a);
     *num_blocks = (int32_t)blocks_needed > nb ? (int32_t)blocks_needed : nb;
     *n_pairs = k;
+    return PKV_OK;
+}
+
+pkv_status pkv_alloc_append_batch(pkv_allocator* a, int32_t* tables, int32_t* num_blocks,
+                                  int32_t S, int32_t MB, const int32_t* ctx_before,
+                                  const int32_t* n_new, int32_t bs, int64_t* pairs,
+                                  int32_t max_pairs, int32_t* n_pairs, int32_t* n_done) {
+    pkv::clear_error();
+    if (!a || S < 0 || MB < 0 || (S > 0 && (!num_blocks || !ctx_before || !n_new)) ||
+        (S > 0 && MB > 0 && !tables) || !n_pairs || !n_done || max_pairs < 0 ||
+        (max_pairs > 0 && !pairs))
+        return pkv::fail(PKV_ERR_INVALID_ARG, "alloc_append_batch: bad argument");
+    *n_pairs = 0;
+    *n_done = 0;
+    int64_t one[2 * 64];
+    for (int32_t s = 0; s < S; ++s) {
+        // one sequence's copies fit in ceil(n_new/bs) + 1 pairs
+        const int64_t cap = (int64_t)n_new[s] / (bs > 0 ? bs : 1) + 2;
+        std::vector<int64_t> big;
+        int64_t* buf = one;
+        if (cap > 64) {
+            big.resize(2 * cap);
+            buf = big.data();
+        }
+        // refuse before touching sequence s if its copies might not fit
+        if (*n_pairs + cap > max_pairs)
+            return pkv::fail(PKV_ERR_INVALID_ARG, "alloc_append_batch: pairs buffer too small");
+        int32_t np = 0;
+        int32_t nb = num_blocks[s];
+        pkv_status st = pkv_alloc_append(a, tables + (int64_t)s * MB, &nb, MB, ctx_before[s],
+                                         n_new[s], bs, buf, &np);
+        if (st != PKV_OK) return st;  // error text already set; nothing changed for s
+        num_blocks[s] = nb;
+        for (int32_t k = 0; k < np; ++k) {
+            pairs[2 * (*n_pairs + k)] = buf[2 * k];
+            pairs[2 * (*n_pairs + k) + 1] = buf[2 * k + 1];
+        }
+        *n_pairs += np;
+        *n_done = s + 1;
+    }
+    return PKV_OK;
+}
+
+pkv_status pkv_alloc_fork(pkv_allocator* a, int32_t* tables, int32_t* num_blocks, int32_t S,
+                          int32_t MB, const int32_t* parents) {
+    pkv::clear_error();
+    if (!a || S < 0 || MB < 0 || (S > 0 && (!num_blocks || !parents)) || (S > 0 && MB > 0 && !tables))
+        return pkv::fail(PKV_ERR_INVALID_ARG, "alloc_fork: bad argument");
+    for (int32_t s = 0; s < S; ++s) {
+        if (parents[s] < 0 || parents[s] >= S || num_blocks[s] < 0 || num_blocks[s] > MB)
+            return pkv::fail(PKV_ERR_INVALID_ARG, "alloc_fork: bad parent or row length");
+        for (int32_t j = 0; j < num_blocks[s]; ++j) {
+            const int32_t id = tables[(int64_t)s * MB + j];
+            if (!valid_id(a, id) || a->rc[id] <= 0)
+                return pkv::fail(PKV_ERR_INVALID_ARG, "alloc_fork: table holds a block that is not held");
+        }
+    }
+    // releases must not underflow: a block released k times by the old rows
+    // needs rc + (holds the new rows take) >= k
+    std::vector<int32_t> old_tab((size_t)S * MB), old_nb(num_blocks, num_blocks + S);
+    std::copy(tables, tables + (size_t)S * MB, old_tab.begin());
+    for (int32_t s = 0; s < S; ++s)
+        for (int32_t j = 0; j < old_nb[parents[s]]; ++j) a->rc[old_tab[(size_t)parents[s] * MB + j]] += 1;
+    for (int32_t s = 0; s < S; ++s)
+        for (int32_t j = 0; j < old_nb[s]; ++j) a->rc[old_tab[(size_t)s * MB + j]] -= 1;
+    bool ok = true;
+    for (int32_t s = 0; s < S && ok; ++s)
+        for (int32_t j = 0; j < old_nb[s]; ++j) ok = ok && a->rc[old_tab[(size_t)s * MB + j]] >= 0;
+    // undo the probe, then apply for real through set_rc / push
+    for (int32_t s = 0; s < S; ++s)
+        for (int32_t j = 0; j < old_nb[s]; ++j) a->rc[old_tab[(size_t)s * MB + j]] += 1;
+    for (int32_t s = 0; s < S; ++s)
+        for (int32_t j = 0; j < old_nb[parents[s]]; ++j) a->rc[old_tab[(size_t)parents[s] * MB + j]] -= 1;
+    if (!ok) return pkv::fail(PKV_ERR_INVALID_ARG, "alloc_fork: release would underflow a refcount");
+    for (int32_t s = 0; s < S; ++s)
+        for (int32_t j = 0; j < old_nb[parents[s]]; ++j) {
+            const int32_t id = old_tab[(size_t)parents[s] * MB + j];
+            set_rc(a, id, a->rc[id] + 1);
+        }
+    for (int32_t s = 0; s < S; ++s)
+        for (int32_t j = 0; j < old_nb[s]; ++j) {
+            const int32_t id = old_tab[(size_t)s * MB + j];
+            set_rc(a, id, a->rc[id] - 1);
+            if (a->rc[id] == 0) push(a, id);
+        }
+    for (int32_t s = 0; s < S; ++s) {
+        const int32_t p = parents[s];
+        std::copy(old_tab.begin() + (size_t)p * MB, old_tab.begin() + (size_t)(p + 1) * MB,
+                  tables + (size_t)s * MB);
+        num_blocks[s] = old_nb[p];
+    }
     return PKV_OK;
 }
 

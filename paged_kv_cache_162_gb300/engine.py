@@ -13,6 +13,7 @@ The step, in the order a serving loop runs it ("3.3 页面级显存管理" 3.3.2
 from __future__ import annotations
 
 import math
+import time
 
 import numpy as np
 import torch
@@ -187,6 +188,102 @@ class DecodeStep:
         if attention:
             self.decode(stream)
         return self.out
+
+    def _beam_buffers(self):
+        """Two pinned staging slots (int32 ints, int64 pairs, 16-bit tokens)
+        and their device twins, so each step uploads with three async
+        copies; an event per slot keeps a slot from being overwritten while
+        its copy may still be in flight."""
+        S, MB, H, D = self.S, self.MB, self.H, self.D
+        n32 = S * MB + 2 * S
+        n64 = 2 * 2 * S          # at most 2 copies per sequence and step
+        n16 = 3 * S * H * D
+        dev = self.device
+        self._beam_slots = []
+        for _ in range(2):
+            self._beam_slots.append({
+                "i32": torch.empty(n32, dtype=torch.int32).pin_memory(),
+                "i64": torch.empty(n64, dtype=torch.int64).pin_memory(),
+                "u16": torch.empty(n16, dtype=torch.int16).pin_memory(),
+                "done": None})
+        self._beam_dev = {"i32": torch.empty(n32, dtype=torch.int32, device=dev),
+                          "i64": torch.empty(n64, dtype=torch.int64, device=dev),
+                          "u16": torch.empty(n16, dtype=torch.int16, device=dev)}
+        self._beam_turn = 0
+        if self.slot_mapping.numel() < S:
+            self.slot_mapping = torch.empty(S, dtype=torch.int64, device=dev)
+
+    def beam_step(self, parents, new_k, new_v, q, stream=None):
+        """One beam-search step after plan(): every sequence b continues from
+        sequence parents[b] (fork: share the parent's blocks), appends one
+        token (copy-on-write of its shared partial block first), then the
+        device copies, writes and attends.  new_k/new_v/q: [S, H, D] uint16
+        bit patterns.  Returns the (src, dst) copy pairs of the step."""
+        S, MB, H, D, bs = self.S, self.MB, self.H, self.D, self.bs
+        if not hasattr(self, "beam_ctx"):
+            self.beam_ctx = self.context_lens_host.astype(np.int32).copy()
+            self.nblocks_host = np.ascontiguousarray(self.nblocks_host, dtype=np.int32)
+            self._beam_buffers()
+        # host: fork (share the parents' blocks) and append, two native calls
+        t0 = time.perf_counter()
+        parents = np.asarray(parents, dtype=np.int64)
+        self.allocator.fork(self.tables_host, self.nblocks_host, parents)
+        ctx = self.beam_ctx[parents]
+        pairs = self.allocator.append_batch(self.tables_host, self.nblocks_host, ctx,
+                                            np.ones(S, dtype=np.int32), bs)
+        self.last_allocator_seconds = time.perf_counter() - t0
+        self.beam_ctx = ctx + 1
+        self.pairs_host = pairs
+        self.context_lens_host = self.beam_ctx
+        self.max_context_len = max(int(self.beam_ctx.max()), 1)
+        P = len(pairs)
+        # stage in pinned memory, then three async copies on the stream
+        slot = self._beam_slots[self._beam_turn]
+        self._beam_turn ^= 1
+        if slot["done"] is not None:
+            slot["done"].synchronize()
+        i32 = slot["i32"].numpy()
+        i32[:S * MB] = self.tables_host.ravel()
+        i32[S * MB:S * MB + S] = self.beam_ctx
+        i32[S * MB + S:] = ctx
+        if P:
+            slot["i64"].numpy()[:2 * P] = pairs.ravel()
+        u16 = slot["u16"].numpy().view(np.uint16)
+        n = S * H * D
+        u16[:n] = np.asarray(q).ravel()
+        u16[n:2 * n] = np.asarray(new_k).ravel()
+        u16[2 * n:] = np.asarray(new_v).ravel()
+        st = stream if stream is not None else torch.cuda.current_stream()
+        d = self._beam_dev
+        with torch.cuda.stream(st):
+            d["i32"].copy_(slot["i32"], non_blocking=True)
+            if P:
+                d["i64"][:2 * P].copy_(slot["i64"][:2 * P], non_blocking=True)
+            d["u16"].copy_(slot["u16"], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(st)
+        slot["done"] = ev
+        self.block_tables = d["i32"][:S * MB].view(S, MB)
+        self.context_lens = d["i32"][S * MB:S * MB + S]
+        self.pos = d["i32"][S * MB + S:S * MB + 2 * S]
+        if getattr(self, "_beam_seq_idx", None) is None:
+            self._beam_seq_idx = torch.arange(S, dtype=torch.int32, device=self.device)
+        self.seq_idx = self._beam_seq_idx
+        tok = d["u16"].view(self.dtype)
+        self.q = tok[:n].view(S, H, D)
+        self.new_k = tok[n:2 * n].view(S, H, D)
+        self.new_v = tok[2 * n:].view(S, H, D)
+        self.T = S
+        need = workspace_size(S, H, D, self.max_context_len, self.partition_tokens)
+        if self.workspace.numel() < need:
+            self.workspace = torch.empty(need, dtype=torch.uint8, device=self.device)
+        if P:
+            self.pairs = d["i64"][:2 * P].view(P, 2)
+            copy_blocks(self.k_cache, self.v_cache, self.pairs, st)
+        compute_slot_mapping(self.slot_mapping, self.block_tables, self.seq_idx, self.pos, bs, st)
+        reshape_and_cache(self.new_k, self.new_v, self.k_cache, self.v_cache, self.slot_mapping, st)
+        self.decode(st)
+        return pairs
 
     def decode(self, stream=None):
         L.pkv_paged_attention_decode(self.out, self.q, self.k_cache, self.v_cache,

@@ -1,0 +1,32 @@
+"""Beam search over the paged cache (fork + copy-on-write every step)
+through the C ABI, step by step against the oracle: tables, copy pairs,
+slots and every cache block bit-exact, attention within tolerance."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import step as OS
+from tests.gpu_harness import assert_attention_close, device_step
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("bs", [16, 8])
+def test_beam_search_steps_match_oracle(bs):
+    bw = W.beam_search(seed=7 + bs, requests=3, beams=4, prompt_lo=20, prompt_hi=70, steps=6,
+                       H=4, D=64, bs=bs)
+    st = device_step(bw.init, 32)
+    st.plan()
+    copies = 0
+    for i, (bt, pairs, slots, k_pool, v_pool, ids, out) in enumerate(OS.run_beam(bw, nthreads=2)):
+        got_pairs = st.beam_step(bw.parents[i], bw.new_k[i], bw.new_v[i], bw.q[i])
+        torch.cuda.synchronize()
+        assert np.array_equal(st.tables_host, bt), f"step {i}: tables"
+        assert np.array_equal(got_pairs, pairs), f"step {i}: pairs"
+        assert np.array_equal(st.slot_mapping[:bw.init.S].cpu().numpy(), slots), f"step {i}"
+        for cache, pool in ((st.k_cache, k_pool), (st.v_cache, v_pool)):
+            assert np.array_equal(cache.view(torch.int16).cpu().numpy().view(np.uint16), pool)
+        assert_attention_close(st.out.float().cpu().double().numpy(), out, f"beam step {i}")
+        copies += len(pairs)
+    assert copies > 0  # forks made shared partial blocks that had to be copied

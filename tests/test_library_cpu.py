@@ -203,3 +203,62 @@ def test_library_allocator_create_with_order_pops_last_first():
     assert a.num_free == 3 and a.refcount(0) == 1 and a.refcount(3) == 0
     assert a.alloc(2) == [1, 8]
     assert a.decref([0]) == 1 and a.alloc(1) == [0]
+
+
+def test_library_beam_fork_matches_model_at_full_size():
+    """16 requests x 4 beams, LLaMA-7B-shaped pool, 8 steps of native fork +
+    append_batch: the same tables, copies, free and shared counts as the
+    model's fork_tables + append."""
+    import workloads as W
+    from oracle.allocator import fork_tables as model_fork
+    from oracle.step import rebuild_allocator
+
+    bw = W.beam_search()
+    w = bw.init
+    mod = rebuild_allocator(w)
+    lib = BlockAllocator(w.NB, w.initial_free)
+    ids, counts = np.unique(w.tables_pre[w.tables_pre >= 0], return_counts=True)
+    for b, c in zip(ids.tolist(), counts.tolist()):
+        if c > 1:
+            lib.incref([b] * (c - 1))
+    tm = [w.tables_pre[s, :w.nblocks_pre[s]].tolist() for s in range(w.S)]
+    tl = np.ascontiguousarray(w.tables_pre.copy())
+    nbl = np.ascontiguousarray(w.nblocks_pre.astype(np.int32))
+    ctx = w.ctx_before.astype(np.int64)
+    total_pairs = 0
+    for i in range(bw.steps):
+        tm = model_fork(mod, tm, bw.parents[i])
+        lib.fork(tl, nbl, bw.parents[i])
+        ctx = ctx[bw.parents[i]]
+        pm = []
+        for b in range(w.S):
+            pm += mod.append(tm[b], int(ctx[b]), 1, w.bs)
+        pl = lib.append_batch(tl, nbl, ctx, np.ones(w.S), w.bs)
+        assert [tuple(p) for p in pl.tolist()] == pm
+        total_pairs += len(pm)
+        ctx += 1
+        for b in range(w.S):
+            assert tl[b, :nbl[b]].tolist() == tm[b]
+        assert mod.num_free == lib.num_free and mod.num_shared == lib.num_shared
+    assert total_pairs > 0
+
+
+def test_library_fork_and_append_batch_errors():
+    a = BlockAllocator(6)
+    t = np.full((2, 4), -1, np.int32)
+    nb = np.zeros(2, np.int32)
+    a.append_batch(t, nb, [0, 0], [20, 10], 16)          # rows: 2 blocks and 1 block
+    assert nb.tolist() == [2, 1] and a.num_free == 3
+    before = (t.copy(), nb.copy(), a.num_free)
+    with pytest.raises(L.PkvError):
+        a.fork(t, nb, [0, 2])                              # parent out of range: nothing changes
+    assert np.array_equal(t, before[0]) and np.array_equal(nb, before[1]) and a.num_free == 3
+    a.fork(t, nb, [0, 0])                                  # both rows share row 0's blocks
+    assert nb.tolist() == [2, 2] and a.num_free == 4 and a.num_shared == 2
+    # 40 more tokens each: row 0 copies its shared partial block and takes 2
+    # new blocks (1 left); row 1 then owns its partial block alone but needs
+    # 2 new blocks: out of blocks, row 1 untouched
+    with pytest.raises(OutOfBlocks):
+        a.append_batch(t, nb, [20, 20], [40, 40], 16)
+    assert nb.tolist() == [4, 2] and a.num_free == 1
+    assert t[1, :2].tolist() == t[0, :1].tolist() + [t[1, 1]] and t[1, 2] == -1

@@ -364,3 +364,63 @@ def small_case(seed, dtype=F16, S=3, H=2, D=64, bs=16, ctx_lo=1, ctx_hi=80, NB=N
     """Small random case for exhaustive parity (several tiles, ragged tails)."""
     return uniform_decode(f"small_{dtype}_D{D}_bs{bs}", seed, dtype, S=S, H=H, D=D, bs=bs,
                           ctx_lo=ctx_lo, ctx_hi=ctx_hi, NB=NB, n_new=n_new, ctx=ctx)
+
+
+@dataclass
+class BeamWorkload:
+    """Beam search over paged KV (fork + copy-on-write every step).
+
+    `init` is the state after the prompts were prefilled: request r's prompt
+    blocks are referenced by all `beams` sequences of the request
+    (sequences r*beams .. r*beams + beams-1).  Then `steps` decode steps:
+    at step i every beam b continues from beam parents[i, b] of its own
+    request (it forks the parent's table), then appends one token with K/V
+    new_k[i, b] / new_v[i, b] and attends with query q[i, b].
+    """
+    init: Workload
+    beams: int
+    parents: np.ndarray   # [steps, S] int32 (sequence index of the parent)
+    new_k: np.ndarray     # [steps, S, H, D] uint16
+    new_v: np.ndarray
+    q: np.ndarray         # [steps, S, H, D] uint16
+
+    @property
+    def steps(self) -> int:
+        return self.parents.shape[0]
+
+
+def beam_search(seed=1006, requests=16, beams=4, prompt_lo=256, prompt_hi=1024, steps=8,
+                H=32, D=128, bs=16, dtype=F16, pool_slack=1.25) -> BeamWorkload:
+    """Beam search, fp16: `requests` prompts x `beams` beams (LLaMA-7B layer
+    shape by default); prompts ~ U{prompt_lo..prompt_hi}; parents drawn
+    uniformly among the request's beams at every step."""
+    r_len, r_perm, r_kv, r_q, r_new, r_par = _streams(seed, 6)
+    S = requests * beams
+    plen = r_len.integers(prompt_lo, prompt_hi + 1, size=requests).astype(np.int64)
+    pre_blocks = _cdiv(plen, bs)
+    MB = int(_cdiv(plen.max() + steps, bs))
+    # prompts once; every step each beam may need a copy of its last block
+    # and at most one new block
+    need = int(pre_blocks.sum()) + S * (2 + 2 * _cdiv(steps, bs).item() + steps)
+    NB = int(need * pool_slack)
+    perm = r_perm.permutation(NB).astype(np.int32)
+    tables = np.full((S, MB), -1, dtype=np.int32)
+    nb_pre = np.zeros(S, dtype=np.int64)
+    k = 0
+    for r in range(requests):
+        shared = perm[k:k + pre_blocks[r]]
+        k += pre_blocks[r]
+        for j in range(beams):
+            s = r * beams + j
+            tables[s, :pre_blocks[r]] = shared
+            nb_pre[s] = pre_blocks[r]
+    ctx_before = np.repeat(plen, beams)
+    init = _finish("beam_search", dtype, S, H, D, bs, NB, MB, ctx_before,
+                   np.zeros(S, dtype=np.int64), tables, nb_pre.astype(np.int32), perm[k:],
+                   (r_kv, r_q, r_new), notes={"prompt_len": plen.tolist()})
+    base = (np.arange(S) // beams) * beams
+    parents = (base[None, :] + r_par.integers(0, beams, size=(steps, S))).astype(np.int32)
+    new_k = normal_bits(r_new, (steps, S, H, D), dtype)
+    new_v = normal_bits(r_new, (steps, S, H, D), dtype)
+    q = normal_bits(r_q, (steps, S, H, D), dtype)
+    return BeamWorkload(init=init, beams=beams, parents=parents, new_k=new_k, new_v=new_v, q=q)
