@@ -47,6 +47,8 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="llama7b_batch64")
     p.add_argument("--partition-tokens", type=int, default=0)
+    p.add_argument("--shared-prefix", action="store_true",
+                   help="shared_prefix workloads: decode with each prompt's prefix read once")
     p.add_argument("--block-size", type=int, default=0,
                    help="llama7b_batch64 only: another block size (8, 16, 32, 64)")
     p.add_argument("--e2e-steps", type=int, default=200)
@@ -320,6 +322,20 @@ def run_ours(args):
     from paged_kv_cache_162_gb300.engine import (StepGraph, compute_slot_mapping, copy_blocks,
                                                  reshape_and_cache)
     has_pairs = len(st.pairs_host) > 0
+    if args.shared_prefix:
+        if not w.name.startswith("shared_prefix"):
+            raise SystemExit("--shared-prefix needs a shared_prefix workload")
+        from paged_kv_cache_162_gb300.engine import paged_attention_decode_shared_prefix
+        samples = w.notes["samples"]
+        groups = torch.tensor([[p * samples, samples, 1024] for p in range(w.S // samples)],
+                              dtype=torch.int32, device=dev)
+        from paged_kv_cache_162_gb300 import _lib as _L
+        ws_sp = torch.empty(_L.pkv_decode_shared_prefix_workspace_size(
+            w.S, w.H, w.D, groups.shape[0], st.max_context_len, args.partition_tokens),
+            dtype=torch.uint8, device=dev)
+        st.decode = lambda stream=None: paged_attention_decode_shared_prefix(
+            st.out, st.q, st.k_cache, st.v_cache, st.block_tables, st.context_lens, groups,
+            st.scale, st.max_context_len, args.partition_tokens, workspace=ws_sp, stream=stream)
 
     def step():
         if has_pairs:

@@ -64,6 +64,7 @@ typedef enum { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype;
 #define PKV_DEVERR_SLOT 0x2      /* slot outside [0, NB*bs) (and >= 0)    */
 #define PKV_DEVERR_CONTEXT 0x4   /* context_len < 0 or > max context      */
 #define PKV_DEVERR_POSITION 0x8  /* slot mapping: position past the table */
+#define PKV_DEVERR_GROUP 0x10    /* shared-prefix group out of range      */
 
 /* Thread-local text of the last error ("" if none).  Never NULL. */
 const char* pkv_last_error_string(void);
@@ -116,6 +117,34 @@ pkv_status pkv_paged_attention_decode(
     int S, int H, int D, int bs, int NB, int MB, int max_context_len,
     float scale, pkv_dtype dtype, int partition_tokens,
     void* workspace, size_t workspace_bytes, void* stream);
+
+/* Decode attention where groups of sequences share a prefix (parallel
+ * sampling, beam search, a common system prompt: [P1] 3.3.2 "Copy-on-Write
+ * 页面共享机制", [P3] 3.1.5, [P4] "Memory Sharing与写时复制").  Computes exactly
+ * what pkv_paged_attention_decode computes; the shared prefix of each group
+ * is read from HBM once for all its members and its q.K and P.V run on the
+ * tensor cores with the members' queries as one matrix.
+ *
+ *   prefix_groups  [G][3] int32, device memory: (first sequence, number of
+ *                  members n in 1..16, prefix tokens).  The members are the
+ *                  sequences first .. first+n-1; their block tables must hold
+ *                  the same physical blocks for the first `prefix tokens`
+ *                  tokens (a multiple of 16, at most each member's context).
+ *                  Groups must not overlap; other sequences are decoded as
+ *                  usual.
+ *   other arguments as in pkv_paged_attention_decode, except that the
+ *   workspace needs pkv_decode_shared_prefix_workspace_size(S, H, D, G,
+ *   max_context_len, partition_tokens) bytes.
+ * Only whole partitions inside a prefix are shared; a prefix shorter than a
+ * partition is decoded as usual. */
+size_t pkv_decode_shared_prefix_workspace_size(int S, int H, int D, int G, int max_context_len,
+                                               int partition_tokens);
+pkv_status pkv_paged_attention_decode_shared_prefix(
+    void* out, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, const int32_t* context_lens, const int32_t* prefix_groups,
+    int G, int S, int H, int D, int bs, int NB, int MB, int max_context_len, float scale,
+    pkv_dtype dtype, int partition_tokens, void* workspace, size_t workspace_bytes,
+    void* stream);
 
 /* Size of the scratch array built into the library for
  * pkv_paged_attention_decode_noalloc: 16 MiB per device. */

@@ -27,6 +27,7 @@ PKV_DEVERR_BLOCK_ID = 0x1
 PKV_DEVERR_SLOT = 0x2
 PKV_DEVERR_CONTEXT = 0x4
 PKV_DEVERR_POSITION = 0x8
+PKV_DEVERR_GROUP = 0x10
 PKV_NOALLOC_SCRATCH_BYTES = 16 << 20
 PKV_SWAP_OUT = 0
 PKV_SWAP_IN = 1
@@ -58,6 +59,9 @@ SIGNATURES = {
     "pkv_decode_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "pkv_paged_attention_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
                                         _I, _P, _SZ, _P]),
+    "pkv_decode_shared_prefix_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "pkv_paged_attention_decode_shared_prefix": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
+                                                      _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P]),
     "pkv_paged_attention_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                                 _I, _F, _I, _I, _P]),
     "pkv_compute_slot_mapping": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P]),
@@ -151,6 +155,22 @@ def pkv_paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_l
         ptr(out), ptr(q), ptr(k_cache), ptr(v_cache), ptr(block_tables), ptr(context_lens), S, H,
         D, bs, NB, MB, max_context_len, float(scale), int(dtype), partition_tokens, ptr(workspace),
         int(workspace_bytes), stream_handle(stream)), "paged_attention_decode")
+
+
+def pkv_decode_shared_prefix_workspace_size(S, H, D, G, max_context_len, partition_tokens=0):
+    return int(lib().pkv_decode_shared_prefix_workspace_size(S, H, D, G, max_context_len,
+                                                             partition_tokens))
+
+
+def pkv_paged_attention_decode_shared_prefix(out, q, k_cache, v_cache, block_tables, context_lens,
+                                             prefix_groups, G, S, H, D, bs, NB, MB,
+                                             max_context_len, scale, dtype, partition_tokens,
+                                             workspace, workspace_bytes, stream=None) -> None:
+    check(lib().pkv_paged_attention_decode_shared_prefix(
+        ptr(out), ptr(q), ptr(k_cache), ptr(v_cache), ptr(block_tables), ptr(context_lens),
+        ptr(prefix_groups), G, S, H, D, bs, NB, MB, max_context_len, float(scale), int(dtype),
+        partition_tokens, ptr(workspace), int(workspace_bytes), stream_handle(stream)),
+        "paged_attention_decode_shared_prefix")
 
 
 def pkv_paged_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, S, H,

@@ -64,6 +64,10 @@ struct Workspace {
     unsigned* counter;  // next work item
     int* n_items;       // number of (sequence, partition) items
     int* pt;            // tokens per partition chosen by the plan kernel
+    unsigned* pcounter; // next prefix item (shared-prefix decode)
+    int* n_pitems;      // number of (group, partition) prefix items
+    int* pitems;        // packed (group << 16 | partition)
+    int* pre_parts;     // per sequence: leading partitions its group's prefix covers
     int* items;         // packed (sequence << 16 | partition)
     int* nparts;        // partitions per sequence
     unsigned* tickets;  // per (sequence, head group): partitions finished
@@ -73,7 +77,7 @@ struct Workspace {
 };
 
 struct Layout {
-    size_t items, nparts, tickets, m, l, acc, total;
+    size_t items, nparts, tickets, m, l, acc, pre_parts, pitems, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -89,6 +93,18 @@ Layout layout_of(int S, int H, int D, int max_parts) {
     L.m = o;       o = align256(o + part_elems * sizeof(float));
     L.l = o;       o = align256(o + part_elems * sizeof(float));
     L.acc = o;     o = align256(o + part_elems * D * sizeof(float));
+    L.pre_parts = L.pitems = 0;
+    L.total = o;
+    return L;
+}
+
+// The decode layout plus what shared-prefix decode needs: per-sequence
+// prefix partition counts and the list of (group, partition) items.
+Layout layout_shared(int S, int H, int D, int G, int max_parts) {
+    Layout L = layout_of(S, H, D, max_parts);
+    size_t o = L.total;
+    L.pre_parts = o; o = align256(o + (size_t)S * sizeof(int));
+    L.pitems = o;    o = align256(o + (size_t)(G > 0 ? G : 1) * max_parts * sizeof(int));
     L.total = o;
     return L;
 }
@@ -99,6 +115,10 @@ Workspace bind(void* base, const Layout& L) {
     w.counter = reinterpret_cast<unsigned*>(b);
     w.n_items = reinterpret_cast<int*>(b + 4);
     w.pt = reinterpret_cast<int*>(b + 8);
+    w.pcounter = reinterpret_cast<unsigned*>(b + 12);
+    w.n_pitems = reinterpret_cast<int*>(b + 16);
+    w.pre_parts = L.pre_parts ? reinterpret_cast<int*>(b + L.pre_parts) : nullptr;
+    w.pitems = L.pitems ? reinterpret_cast<int*>(b + L.pitems) : nullptr;
     w.items = reinterpret_cast<int*>(b + L.items);
     w.nparts = reinterpret_cast<int*>(b + L.nparts);
     w.tickets = reinterpret_cast<unsigned*>(b + L.tickets);
@@ -136,7 +156,9 @@ __device__ __forceinline__ int clamp_ctx(int c, int max_ctx) {
 __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const int32_t* __restrict__ context_lens,
                                                                 int S, int pt_fixed, int pt_min,
                                                                 int max_ctx, int slots, int HG,
-                                                                int n_tickets, Workspace ws, int* err) {
+                                                                int n_tickets, Workspace ws,
+                                                                const int32_t* __restrict__ groups,
+                                                                int G, int* err) {
     constexpr int kWarpsP = kPlanThreads / 32;
     constexpr int kVals = 2 * kAutoCandidates + 1;  // full and all per candidate, sum of contexts
     // context_lens may come from the kernel before this one
@@ -211,16 +233,52 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const int32_t* __
     __syncthreads();
     const int PT = s_pt;
 
+    // shared prefixes: every member of group g skips the first pp_g
+    // partitions, which the prefix kernel computes for all members at once
+    __shared__ int s_full_skip, s_pitems;
+    if (G > 0) {
+        for (int s = tid; s < S; s += kPlanThreads) ws.pre_parts[s] = 0;
+        if (tid == 0) { s_full_skip = 0; s_pitems = 0; }
+        __syncthreads();
+        for (int g = tid; g < G; g += kPlanThreads) {
+            const int first = groups[3 * g], n = groups[3 * g + 1], ptok = groups[3 * g + 2];
+            if (first < 0 || n < 1 || n > 16 || first > S - n || ptok < 0 || ptok % kTile) {
+                pkv::report(err, PKV_DEVERR_GROUP);
+                continue;
+            }
+            int pp = ptok / PT;
+            for (int j = 0; j < n; ++j) pp = min(pp, clamp_ctx(context_lens[first + j], max_ctx) / PT);
+            for (int j = 0; j < n; ++j) ws.pre_parts[first + j] = pp;
+            atomicAdd(&s_full_skip, pp * n);
+            atomicAdd(&s_pitems, pp);
+        }
+        __syncthreads();
+        if (tid == 0) {
+            // prefix items in group order (serial: groups are few)
+            int k = 0;
+            for (int g = 0; g < G; ++g) {
+                const int first = groups[3 * g], n = groups[3 * g + 1], ptok = groups[3 * g + 2];
+                if (first < 0 || n < 1 || n > 16 || first > S - n || ptok < 0 || ptok % kTile) continue;
+                const int pp = ws.pre_parts[first];
+                for (int part = 0; part < pp; ++part) ws.pitems[k++] = (g << 16) | part;
+            }
+            s_full_total -= s_full_skip;
+            s_items -= s_full_skip;
+        }
+        __syncthreads();
+    }
+
     // item list: full partitions first (sequence order), partial ones after
     for (int base = 0; base < S; base += kPlanThreads) {
         const int s = base + tid;
-        int nf = 0, np = 0;
+        int nf = 0, np = 0, skip = 0;
         if (s < S) {
             const int c = clamp_ctx(context_lens[s], max_ctx);
             nf = c / PT;
             np = (c % PT != 0 || c == 0) ? 1 : 0;  // an empty context still writes zeros
+            skip = G > 0 ? ws.pre_parts[s] : 0;
         }
-        int a = nf, b = np;
+        int a = nf - skip, b = np;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int x = __shfl_up_sync(kFull, a, o), y = __shfl_up_sync(kFull, b, o);
@@ -228,15 +286,15 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const int32_t* __
         }
         if (lane == 31) { wsum[0][wid] = a; wsum[1][wid] = b; }
         __syncthreads();
-        int off_f = carry[0] + a - nf, off_p = carry[1] + b - np;
+        int off_f = carry[0] + a - (nf - skip), off_p = carry[1] + b - np;
         for (int w = 0; w < wid; ++w) { off_f += wsum[0][w]; off_p += wsum[1][w]; }
         if (s < S) {
-            for (int k = 0; k < nf; ++k) ws.items[off_f + k] = (s << 16) | k;
+            for (int k = skip; k < nf; ++k) ws.items[off_f + k - skip] = (s << 16) | k;
             if (np) ws.items[s_full_total + off_p] = (s << 16) | nf;
             ws.nparts[s] = nf + np;
         }
         __syncthreads();
-        if (tid == kPlanThreads - 1) { carry[0] = off_f + nf; carry[1] = off_p + np; }
+        if (tid == kPlanThreads - 1) { carry[0] = off_f + nf - skip; carry[1] = off_p + np; }
         __syncthreads();
     }
     for (int i = tid; i < n_tickets; i += kPlanThreads) ws.tickets[i] = 0u;
@@ -244,6 +302,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const int32_t* __
         *ws.counter = 0u;
         *ws.n_items = s_items;
         *ws.pt = PT;
+        *ws.pcounter = 0u;
+        *ws.n_pitems = G > 0 ? s_pitems : 0;
     }
 }
 
@@ -562,6 +622,301 @@ __global__ void __launch_bounds__(kThreads, PKV_MIN_CTAS_PER_SM) decode_kernel(D
 }
 
 // ---------------------------------------------------------------------------
+// Shared-prefix decode: one warp computes one head of one prefix partition
+// for all (up to 16) members of a group on the tensor cores.
+//
+// With the members' queries as the rows of Q (M = 16, unused rows zero):
+//   S^T = Q K^T   m16n8k16, A = Q (registers), B = K tile (ldmatrix)
+//   O  += P V     m16n8k16, A = P (the S^T accumulators, rounded to 16 bits:
+//                 the accumulator layout of the first product is the A layout
+//                 of the second), B = V tile (ldmatrix.trans)
+// K/V tiles of 16 tokens stream through a 3-stage cp.async ring per warp in
+// shared memory, 16-byte chunks XOR-swizzled by row so ldmatrix reads are
+// conflict-free.  Each member's (max, sum, output) partial goes to the same
+// workspace slots as the decode kernel's, and the same tickets merge them.
+// ---------------------------------------------------------------------------
+constexpr int kPrefixStages = 3;
+
+template <class E>
+struct Mma;
+template <>
+struct Mma<pkv::F16> {
+    static __device__ __forceinline__ void run(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+};
+template <>
+struct Mma<pkv::BF16> {
+    static __device__ __forceinline__ void run(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+struct PrefixParams {
+    DecodeParams d;
+    const int32_t* groups;  // [G][3]: first sequence, members, prefix tokens
+    int G;
+};
+
+template <class E, int D, int BS>
+__device__ __forceinline__ void prefix_partition(const DecodeParams& a, const int32_t* bt_row,
+                                                 int first, int n, int h, int part, int PT,
+                                                 unsigned char* stage_base, int lane) {
+    constexpr int NK = D / 16;           // k-steps of q.K
+    constexpr int NO = D / 8;            // 8-dim column tiles of the output
+    constexpr int ROWB = D * 2;          // bytes of one K or V row
+    constexpr int TILEB = kTile * ROWB;  // bytes of one K (or V) tile
+    constexpr int CPR = ROWB / 16;       // 16-byte chunks per row
+    constexpr int CPL = kTile * CPR / 32;  // chunks per lane per tile
+    const int g = lane >> 2, t = lane & 3;
+    const int64_t HD = (int64_t)a.H * D;
+
+    // Q fragments: rows = members g and g+8, dims 16k + 2t (+8)
+    uint32_t qa[NK][4];
+    {
+        const uint16_t* q0 = static_cast<const uint16_t*>(a.q) + ((int64_t)(first + g) * a.H + h) * D;
+        const uint16_t* q1 = static_cast<const uint16_t*>(a.q) + ((int64_t)(first + g + 8) * a.H + h) * D;
+        const bool r0 = g < n, r1 = g + 8 < n;
+#pragma unroll
+        for (int k = 0; k < NK; ++k) {
+            qa[k][0] = r0 ? __ldg(reinterpret_cast<const uint32_t*>(q0 + 16 * k + 2 * t)) : 0u;
+            qa[k][1] = r1 ? __ldg(reinterpret_cast<const uint32_t*>(q1 + 16 * k + 2 * t)) : 0u;
+            qa[k][2] = r0 ? __ldg(reinterpret_cast<const uint32_t*>(q0 + 16 * k + 8 + 2 * t)) : 0u;
+            qa[k][3] = r1 ? __ldg(reinterpret_cast<const uint32_t*>(q1 + 16 * k + 8 + 2 * t)) : 0u;
+        }
+    }
+    const uint16_t* k_head = static_cast<const uint16_t*>(a.k_cache) + (int64_t)h * D;
+    const uint16_t* v_head = static_cast<const uint16_t*>(a.v_cache) + (int64_t)h * D;
+    const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(stage_base));
+    const int t_begin = part * PT, ntiles = PT / kTile;
+
+    // issue the copies of tile i into stage i % kPrefixStages
+    auto issue = [&](int i) {
+        if (i < ntiles) {
+            const int t0 = t_begin + i * kTile;
+            const uint32_t sk = sbase + (i % kPrefixStages) * 2 * TILEB, sv = sk + TILEB;
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) {
+                const int chunk = lane + 32 * j;
+                const int row = chunk / CPR, c = chunk % CPR;
+                const int tok = t0 + row;
+                int phys = __ldg(bt_row + tok / BS);
+                if ((unsigned)phys >= (unsigned)a.NB) {
+                    pkv::report(a.err, PKV_DEVERR_BLOCK_ID);
+                    phys = 0;
+                }
+                const int64_t off = ((int64_t)phys * BS + tok % BS) * HD + c * 8;
+                const uint32_t dst = row * ROWB + ((c ^ (row & 7)) * 16);
+                cp_async16(sk + dst, k_head + off);
+                cp_async16(sv + dst, v_head + off);
+            }
+        }
+        cp_async_commit();  // an empty group past the end keeps the counting simple
+    };
+
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+    float o[NO][4];
+#pragma unroll
+    for (int j = 0; j < NO; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+
+#pragma unroll
+    for (int i = 0; i < kPrefixStages - 1; ++i) issue(i);
+    for (int i = 0; i < ntiles; ++i) {
+        issue(i + kPrefixStages - 1);
+        cp_async_wait<kPrefixStages - 1>();
+        __syncwarp();
+        const uint32_t sk = sbase + (i % kPrefixStages) * 2 * TILEB, sv = sk + TILEB;
+        // S^T = Q K^T: two 8-token column tiles
+        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        {
+            const int mi = lane >> 3, ri = lane & 7;
+            const int row = (mi >> 1) * 8 + ri;
+#pragma unroll
+            for (int k = 0; k < NK; ++k) {
+                uint32_t b[4];
+                const int c = 2 * k + (mi & 1);
+                ldsm_x4(b, sk + row * ROWB + ((c ^ (row & 7)) * 16));
+                Mma<E>::run(sc[0], qa[k], b[0], b[1]);
+                Mma<E>::run(sc[1], qa[k], b[2], b[3]);
+            }
+        }
+        // online softmax per member row (g: [0],[1]; g+8: [2],[3])
+        float mt[2];
+        mt[0] = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1])) * a.qscale;
+        mt[1] = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3])) * a.qscale;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            mt[r] = fmaxf(mt[r], __shfl_xor_sync(kFull, mt[r], 1));
+            mt[r] = fmaxf(mt[r], __shfl_xor_sync(kFull, mt[r], 2));
+        }
+        float corr[2], mu[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const float m_new = fmaxf(m_run[r], mt[r]);
+            corr[r] = exp2f(m_run[r] - m_new);
+            mu[r] = m_new;
+            m_run[r] = m_new;
+        }
+        float p[2][4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            p[j][0] = exp2f(sc[j][0] * a.qscale - mu[0]);
+            p[j][1] = exp2f(sc[j][1] * a.qscale - mu[0]);
+            p[j][2] = exp2f(sc[j][2] * a.qscale - mu[1]);
+            p[j][3] = exp2f(sc[j][3] * a.qscale - mu[1]);
+        }
+        l_run[0] = l_run[0] * corr[0] + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
+        l_run[1] = l_run[1] * corr[1] + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
+#pragma unroll
+        for (int j = 0; j < NO; ++j) {
+            o[j][0] *= corr[0]; o[j][1] *= corr[0];
+            o[j][2] *= corr[1]; o[j][3] *= corr[1];
+        }
+        // P as the A operand: (row g, tokens 2t..), (row g+8, 2t..), (g, 8+2t..), (g+8, 8+2t..)
+        const uint32_t pa[4] = {E::from_float2(p[0][0], p[0][1]), E::from_float2(p[0][2], p[0][3]),
+                                E::from_float2(p[1][0], p[1][1]), E::from_float2(p[1][2], p[1][3])};
+        {
+            const int mi = lane >> 3, ri = lane & 7;
+            const int row = (mi & 1) * 8 + ri;
+#pragma unroll
+            for (int j = 0; j < NO; j += 2) {
+                uint32_t b[4];
+                const int c = j + (mi >> 1);
+                ldsm_x4_trans(b, sv + row * ROWB + ((c ^ (row & 7)) * 16));
+                Mma<E>::run(o[j], pa, b[0], b[1]);
+                Mma<E>::run(o[j + 1], pa, b[2], b[3]);
+            }
+        }
+        __syncwarp();  // the stage may be refilled now
+    }
+    cp_async_wait<0>();
+
+    // per member: sum over the quad, then the partial (or the output)
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        l_run[r] += __shfl_xor_sync(kFull, l_run[r], 1);
+        l_run[r] += __shfl_xor_sync(kFull, l_run[r], 2);
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int member = g + 8 * r;
+        if (member >= n) continue;
+        const int s = first + member;
+        const int np = a.ws.nparts[s];
+        if (np == 1) {
+            const float inv = l_run[r] > 0.f ? 1.f / l_run[r] : 0.f;
+            uint16_t* dst = static_cast<uint16_t*>(a.out) + ((int64_t)s * a.H + h) * D + 2 * t;
+#pragma unroll
+            for (int j = 0; j < NO; ++j)
+                *reinterpret_cast<uint32_t*>(dst + 8 * j) =
+                    E::from_float2(o[j][2 * r] * inv, o[j][2 * r + 1] * inv);
+        } else {
+            const int64_t idx = ((int64_t)s * a.H + h) * a.max_parts + part;
+            float* dst = a.ws.acc + idx * D + 2 * t;
+#pragma unroll
+            for (int j = 0; j < NO; ++j)
+                *reinterpret_cast<float2*>(dst + 8 * j) = make_float2(o[j][2 * r], o[j][2 * r + 1]);
+            if (t == 0) {
+                a.ws.m[idx] = m_run[r];
+                a.ws.l[idx] = l_run[r];
+            }
+        }
+    }
+}
+
+template <class E, int D, int BS>
+__global__ void __launch_bounds__(kThreads, 2) prefix_kernel(PrefixParams pp) {
+    // wait for the plan kernel (programmatic dependent launch)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    extern __shared__ __align__(128) unsigned char prefix_smem[];
+    __shared__ int s_item;
+    __shared__ unsigned s_last;  // bit j: member j's (sequence, head group) completes here
+    const DecodeParams& a = pp.d;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int total = *a.ws.n_pitems * a.HG;
+    const int PT = *a.ws.pt;
+    constexpr int STAGE_BYTES = kPrefixStages * 2 * kTile * D * 2;
+    unsigned char* my_stages = prefix_smem + warp * STAGE_BYTES;
+    if (threadIdx.x == 0) s_item = (int)atomicAdd(a.ws.pcounter, 1u);
+    __syncthreads();
+    int item = s_item;
+    while (item < total) {
+        int next = 0;
+        if (threadIdx.x == 0) next = (int)atomicAdd(a.ws.pcounter, 1u);
+        const int hg = item % a.HG;
+        const int packed = a.ws.pitems[item / a.HG];
+        const int gi = packed >> 16, part = packed & 0xffff;
+        const int first = pp.groups[3 * gi], n = pp.groups[3 * gi + 1];
+        const int h = hg * kWarps + warp;
+        const int32_t* bt_row = a.block_tables + (int64_t)first * a.MB;  // the shared blocks
+        if (h < a.H) prefix_partition<E, D, BS>(a, bt_row, first, n, h, part, PT, my_stages, lane);
+        // tickets of the members that have more than one partition
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x < 16) {
+            const int j = threadIdx.x;
+            unsigned bit = 0;
+            if (j < n) {
+                const int s = first + j;
+                const int np = a.ws.nparts[s];
+                if (np > 1) {
+                    const unsigned done = atomicAdd(&a.ws.tickets[s * a.HG + hg], 1u);
+                    bit = (done == (unsigned)(np - 1)) ? (1u << j) : 0u;
+                }
+            }
+            // gather the 16 bits in warp 0's first half
+#pragma unroll
+            for (int o = 8; o >= 1; o >>= 1) bit |= __shfl_xor_sync(0xffffu, bit, o);
+            if (j == 0) s_last = bit;
+        }
+        __syncthreads();
+        unsigned last = s_last;
+        if (last) {
+            __threadfence();
+            while (last) {
+                const int j = __ffs(last) - 1;
+                last &= last - 1;
+                const int s = first + j;
+                if (h < a.H) merge_partitions<E, D>(a, s, h, a.ws.nparts[s], lane);
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) s_item = next;
+        __syncthreads();
+        item = s_item;
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 using KernelFn = void (*)(DecodeParams);
@@ -583,6 +938,46 @@ KernelFn pick_d(int D, int bs) {
 
 KernelFn pick(pkv_dtype dt, int D, int bs) {
     return dt == PKV_BF16 ? pick_d<pkv::BF16>(D, bs) : pick_d<pkv::F16>(D, bs);
+}
+
+using PrefixFn = void (*)(PrefixParams);
+
+template <class E, int D>
+PrefixFn pick_prefix_bs(int bs) {
+    switch (bs) {
+        case 8: return prefix_kernel<E, D, 8>;
+        case 16: return prefix_kernel<E, D, 16>;
+        case 32: return prefix_kernel<E, D, 32>;
+        default: return prefix_kernel<E, D, 64>;
+    }
+}
+
+PrefixFn pick_prefix(pkv_dtype dt, int D, int bs) {
+    if (dt == PKV_BF16) return D == 64 ? pick_prefix_bs<pkv::BF16, 64>(bs) : pick_prefix_bs<pkv::BF16, 128>(bs);
+    return D == 64 ? pick_prefix_bs<pkv::F16, 64>(bs) : pick_prefix_bs<pkv::F16, 128>(bs);
+}
+
+size_t prefix_smem_bytes(int D) { return (size_t)kWarps * kPrefixStages * 2 * kTile * D * 2; }
+
+// Resident CTAs per SM of the prefix kernel (its shared memory set once).
+int prefix_resident(PrefixFn fn, int D) {
+    static std::mutex mu;
+    static struct { PrefixFn fn; int dev; int n; } cache[64];
+    static int used = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < used; ++i)
+        if (cache[i].fn == fn && cache[i].dev == dev) return cache[i].n;
+    const int smem = (int)prefix_smem_bytes(D);
+    int n = 0;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, smem) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (used < 64) cache[used++] = {fn, dev, n};
+    return n;
 }
 
 int resident_ctas(KernelFn fn) {
@@ -686,7 +1081,8 @@ cudaLaunchAttribute pdl_attr() {
 pkv_status launch_decode(const char* who, const CallShape& cs, void* out, const void* q,
                          const void* k_cache, const void* v_cache, const int32_t* block_tables,
                          const int32_t* context_lens, int S, int H, int D, int bs, int NB, int MB,
-                         float scale, pkv_dtype dtype, void* workspace, cudaStream_t st) {
+                         float scale, pkv_dtype dtype, void* workspace, cudaStream_t st,
+                         const int32_t* groups = nullptr, int G = 0) {
     DecodeParams p;
     p.out = out;
     p.q = q;
@@ -719,10 +1115,30 @@ pkv_status launch_decode(const char* who, const CallShape& cs, void* out, const 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, plan_kernel, context_lens, S, cs.pt_fixed, cs.pt_min,
-                                       cs.max_ctx, grid, p.HG, S * H, p.ws, p.err);
+                                       cs.max_ctx, grid, p.HG, S * H, p.ws, groups, G, p.err);
     if (e != cudaSuccess) {
         snprintf(msg, sizeof msg, "%s plan launch", who);
         return pkv::cuda_fail(e, msg);
+    }
+    if (G > 0) {
+        PrefixFn pfn = pick_prefix(dtype, D, bs);
+        const int per_sm = prefix_resident(pfn, D);
+        if (per_sm < 1) return pkv::fail(PKV_ERR_CUDA, "prefix kernel cannot be resident");
+        const int64_t pupper = (int64_t)G * cs.max_parts * p.HG;
+        const int64_t president = (int64_t)per_sm * pkv::sm_count();
+        PrefixParams pp;
+        pp.d = p;
+        pp.groups = groups;
+        pp.G = G;
+        cfg.gridDim = dim3((unsigned)(pupper < president ? pupper : president));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = prefix_smem_bytes(D);
+        e = cudaLaunchKernelEx(&cfg, pfn, pp);
+        if (e != cudaSuccess) {
+            snprintf(msg, sizeof msg, "%s prefix launch", who);
+            return pkv::cuda_fail(e, msg);
+        }
+        cfg.dynamicSmemBytes = 0;
     }
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
@@ -771,6 +1187,44 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_ca
         return pkv::fail(PKV_ERR_WORKSPACE, "paged_attention_decode: workspace too small");
     return launch_decode(who, cs, out, q, k_cache, v_cache, block_tables, context_lens, S, H, D, bs,
                          NB, MB, scale, dtype, workspace, pkv::as_stream(stream));
+}
+
+size_t pkv_decode_shared_prefix_workspace_size(int S, int H, int D, int G, int max_context_len,
+                                               int partition_tokens) {
+    if (S < 0 || H <= 0 || (D != 64 && D != 128) || G < 0 || max_context_len < 0 ||
+        partition_tokens < 0 || partition_tokens % kTile)
+        return 0;
+    int pt = partition_tokens;
+    if (pt == 0) pt = auto_pt_min(S, H, D, max_context_len, SIZE_MAX);
+    if (pt == 0) return 0;
+    const int mp = max_parts_of(max_context_len, pt);
+    if (mp > 65535) return 0;
+    return layout_shared(S, H, D, G, mp).total;
+}
+
+pkv_status pkv_paged_attention_decode_shared_prefix(
+    void* out, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, const int32_t* context_lens, const int32_t* prefix_groups, int G,
+    int S, int H, int D, int bs, int NB, int MB, int max_context_len, float scale, pkv_dtype dtype,
+    int partition_tokens, void* workspace, size_t workspace_bytes, void* stream) {
+    static const char* who = "paged_attention_decode_shared_prefix";
+    pkv::clear_error();
+    if (G < 0 || G > 32767 || (G > 0 && !prefix_groups))
+        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode_shared_prefix: bad groups");
+    if (S > 0 && workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode_shared_prefix: workspace must be 256-byte aligned");
+    CallShape cs;
+    pkv_status st = check_call(who, out, q, k_cache, v_cache, block_tables, context_lens, S, H, D,
+                               bs, NB, MB, max_context_len, scale, dtype, partition_tokens,
+                               SIZE_MAX, &cs);
+    if (st != PKV_OK || S == 0) return st;
+    cs.L = layout_shared(S, H, D, G, cs.max_parts);
+    if (!workspace) return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode_shared_prefix: null workspace");
+    if (workspace_bytes < cs.L.total)
+        return pkv::fail(PKV_ERR_WORKSPACE, "paged_attention_decode_shared_prefix: workspace too small");
+    return launch_decode(who, cs, out, q, k_cache, v_cache, block_tables, context_lens, S, H, D,
+                         bs, NB, MB, scale, dtype, workspace, pkv::as_stream(stream),
+                         prefix_groups, G);
 }
 
 }  // extern "C"

@@ -67,6 +67,30 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
     return out
 
 
+def paged_attention_decode_shared_prefix(out, q, k_cache, v_cache, block_tables, context_lens,
+                                         prefix_groups, scale=None, max_context_len=0,
+                                         partition_tokens=0, workspace=None, stream=None):
+    """paged_attention_decode where groups of sequences share a prefix
+    (prefix_groups [G, 3] int32 on the device: first sequence, members,
+    prefix tokens); the prefix is read once per group (tensor cores)."""
+    S, H, D = q.shape
+    NB, bs = k_cache.shape[0], k_cache.shape[1]
+    MB = block_tables.shape[1]
+    G = prefix_groups.shape[0]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    mcl = max_context_len or MB * bs
+    need = L.pkv_decode_shared_prefix_workspace_size(S, H, D, G, mcl, partition_tokens)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    L.pkv_paged_attention_decode_shared_prefix(out, q, k_cache, v_cache, block_tables,
+                                               context_lens, prefix_groups, G, S, H, D, bs, NB, MB,
+                                               max_context_len, scale, dtype_code(q.dtype),
+                                               partition_tokens, workspace, workspace.numel(),
+                                               stream)
+    return out
+
+
 def compute_slot_mapping(slot_mapping, block_tables, seq_idx, pos, block_size, stream=None):
     L.pkv_compute_slot_mapping(slot_mapping, block_tables, seq_idx, pos, seq_idx.numel(),
                                block_tables.shape[0], block_tables.shape[1], block_size, stream)
@@ -284,6 +308,14 @@ class DecodeStep:
         reshape_and_cache(self.new_k, self.new_v, self.k_cache, self.v_cache, self.slot_mapping, st)
         self.decode(st)
         return pairs
+
+    def decode_shared_prefix(self, prefix_groups, stream=None):
+        """decode() with the prefix of each group read once (see
+        paged_attention_decode_shared_prefix); prefix_groups [G, 3] int32."""
+        g = torch.as_tensor(np.asarray(prefix_groups, dtype=np.int32)).to(self.device)
+        return paged_attention_decode_shared_prefix(
+            self.out, self.q, self.k_cache, self.v_cache, self.block_tables, self.context_lens, g,
+            self.scale, self.max_context_len, self.partition_tokens, stream=stream)
 
     def decode(self, stream=None):
         L.pkv_paged_attention_decode(self.out, self.q, self.k_cache, self.v_cache,

@@ -1,0 +1,59 @@
+"""Shared-prefix decode (one read of each group's prefix, tensor cores)
+through the C ABI: against the fp64 oracle and against the plain decode
+entry point, for group sizes 1..16, both dtypes, head_dim 64/128 and several
+block sizes, with grouped and ungrouped sequences in one batch."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from tests.gpu_harness import assert_attention_close, compare_step, device_step, out_to_double
+
+pytestmark = pytest.mark.gpu
+
+
+def _groups(w, samples, prefix, every=1):
+    prompts = w.S // samples
+    return np.array([[p * samples, samples, prefix] for p in range(0, prompts, every)],
+                    dtype=np.int32)
+
+
+@pytest.mark.parametrize("dtype", [W.F16, W.BF16])
+@pytest.mark.parametrize("D,bs", [(128, 16), (64, 32), (128, 8)])
+@pytest.mark.parametrize("samples", [1, 3, 8, 16])
+def test_prefix_groups_small(dtype, D, bs, samples):
+    w = W.shared_prefix(seed=samples * 10 + bs + D, prompts=4, samples=samples, prefix=128,
+                        tail_lo=1, tail_hi=90, H=6, D=D, bs=bs, dtype=dtype)
+    r = compare_step(w, partition_tokens=64)           # plain decode vs the oracle
+    st = r["step"]
+    ref = r["ref"].out
+    plain = out_to_double(st.out)
+    st.out.fill_(float("nan"))
+    # every other prompt grouped, the rest decoded as usual
+    st.decode_shared_prefix(_groups(w, samples, 128, every=2))
+    torch.cuda.synchronize()
+    got = out_to_double(st.out)
+    assert_attention_close(got, ref, f"shared prefix {dtype} D{D} bs{bs} n{samples}")
+    np.testing.assert_allclose(got, plain, atol=2e-3, rtol=1e-2)
+
+
+def test_prefix_shorter_than_a_partition_falls_back():
+    w = W.shared_prefix(seed=5, prompts=2, samples=4, prefix=48, tail_lo=1, tail_hi=30, H=4,
+                        D=128)
+    r = compare_step(w, partition_tokens=64)
+    st = r["step"]
+    st.decode_shared_prefix(_groups(w, 4, 48))
+    torch.cuda.synchronize()
+    assert_attention_close(out_to_double(st.out), r["ref"].out, "short prefix")
+
+
+@pytest.mark.parametrize("cow", [False, True])
+def test_shared_prefix_full_workload(cow):
+    """32 prompts x 8 samples sharing a 1024-token prefix (64 blocks)."""
+    w = W.shared_prefix(cow=cow)
+    r = compare_step(w)
+    st = r["step"]
+    st.out.fill_(float("nan"))
+    st.decode_shared_prefix(_groups(w, 8, 1024))
+    torch.cuda.synchronize()
+    assert_attention_close(out_to_double(st.out), r["ref"].out, "shared prefix full")

@@ -293,7 +293,7 @@ def continuous_batching_bf16(seed=1002, S=256, NB=20000, fresh_frac=0.12,
 
 
 def shared_prefix(seed=1003, prompts=32, samples=8, prefix=1024, tail_lo=1, tail_hi=256,
-                  cow=False, pool_slack=0.10) -> Workload:
+                  cow=False, pool_slack=0.10, H=32, D=128, bs=16, dtype=F16) -> Workload:
     """Parallel sampling, fp16: 32 prompts x 8 samples, 32 x 128, bs 16.
 
     cow=False: every sample shares its prompt's 1024-token prefix (64 full
@@ -304,10 +304,9 @@ def shared_prefix(seed=1003, prompts=32, samples=8, prefix=1024, tail_lo=1, tail
     the fork (one token per sample), which must copy that block first.
     """
     r_len, r_perm, r_kv, r_q, r_new = _streams(seed + (100 if cow else 0), 5)
-    bs, H, D = 16, 32, 128
     S = prompts * samples
     if cow:
-        plen = prefix + r_len.integers(1, 16, size=prompts)
+        plen = prefix + r_len.integers(1, min(bs, 16), size=prompts)
         ctx_before = np.repeat(plen, samples).astype(np.int64)
         n_new = np.ones(S, dtype=np.int64)
     else:
@@ -339,7 +338,7 @@ def shared_prefix(seed=1003, prompts=32, samples=8, prefix=1024, tail_lo=1, tail
             k += own
             nb_pre[s] = pre_blocks[p] + own
     free = perm[k:]
-    return _finish("shared_prefix_cow" if cow else "shared_prefix", F16, S, H, D, bs, NB, MB,
+    return _finish("shared_prefix_cow" if cow else "shared_prefix", dtype, S, H, D, bs, NB, MB,
                    ctx_before, n_new, tables, nb_pre.astype(np.int32), free,
                    (r_kv, r_q, r_new), notes={"prompt_len": plen.tolist(), "samples": samples})
 
