@@ -467,7 +467,8 @@ def run_ours(args):
 
     if rank == 0:
         cfg = describe(w)
-        chosen = int(st.workspace[8:12].view(torch.int32).item())  # plan kernel's choice
+        used_ws = ws_sp if args.shared_prefix else st.workspace
+        chosen = int(used_ws[8:12].view(torch.int32).item())  # plan kernel's choice
         cfg.update({"partition_tokens": (f"auto ({chosen})" if not args.partition_tokens
                                          else args.partition_tokens),
                     "l2": f"inputs larger than L2: {kv_bytes / 1e9:.2f} GB of KV read per step "

@@ -212,9 +212,29 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const int32_t* __
         tot[tid] = t;
     }
     __syncthreads();
+    // shared prefixes (automatic size): partitions no longer than the
+    // shortest valid group prefix, so whole partitions can be shared
+    __shared__ int s_min_prefix;
+    if (tid == 0) s_min_prefix = INT32_MAX;
+    __syncthreads();
+    if (G > 0 && !fixed) {
+        for (int g = tid; g < G; g += kPlanThreads) {
+            const int first = groups[3 * g], n = groups[3 * g + 1], ptok = groups[3 * g + 2];
+            if (first >= 0 && n >= 1 && n <= 16 && first <= S - n && ptok >= pt_min && ptok % kTile == 0)
+                atomicMin(&s_min_prefix, ptok);
+        }
+    }
+    __syncthreads();
     if (tid == 0) {
         int pick = 0;
-        if (!fixed) {
+        if (!fixed && G > 0 && s_min_prefix != INT32_MAX) {
+            bool fits = true;
+#pragma unroll
+            for (int k = 1; k < kAutoCandidates; ++k) {
+                fits = fits && (pt_min << k) <= s_min_prefix;
+                if (fits) pick = k;
+            }
+        } else if (!fixed) {
             const long long mean = S > 0 ? tot[2 * kAutoCandidates] / S : 0;
             bool grow = true;
 #pragma unroll
@@ -250,18 +270,13 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const int32_t* __
             for (int j = 0; j < n; ++j) pp = min(pp, clamp_ctx(context_lens[first + j], max_ctx) / PT);
             for (int j = 0; j < n; ++j) ws.pre_parts[first + j] = pp;
             atomicAdd(&s_full_skip, pp * n);
-            atomicAdd(&s_pitems, pp);
+            // this group's prefix items; their order in the list does not
+            // matter (partials are merged in partition order)
+            const int off = atomicAdd(&s_pitems, pp);
+            for (int part = 0; part < pp; ++part) ws.pitems[off + part] = (g << 16) | part;
         }
         __syncthreads();
         if (tid == 0) {
-            // prefix items in group order (serial: groups are few)
-            int k = 0;
-            for (int g = 0; g < G; ++g) {
-                const int first = groups[3 * g], n = groups[3 * g + 1], ptok = groups[3 * g + 2];
-                if (first < 0 || n < 1 || n > 16 || first > S - n || ptok < 0 || ptok % kTile) continue;
-                const int pp = ws.pre_parts[first];
-                for (int part = 0; part < pp; ++part) ws.pitems[k++] = (g << 16) | part;
-            }
             s_full_total -= s_full_skip;
             s_items -= s_full_skip;
         }
