@@ -65,7 +65,6 @@ typedef enum { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype;
 #define PKV_DEVERR_CONTEXT 0x4   /* context_len < 0 or > max context      */
 #define PKV_DEVERR_POSITION 0x8  /* slot mapping: position past the table */
 #define PKV_DEVERR_GROUP 0x10    /* shared-prefix group out of range      */
-#define PKV_DEVERR_TIMEOUT 0x20  /* a bounded wait for a copy gave up      */
 
 /* Thread-local text of the last error ("" if none).  Never NULL. */
 const char* pkv_last_error_string(void);
