@@ -62,3 +62,20 @@ def test_bad_slot_and_position_and_copy_pair():
     E.copy_blocks(k, v, pairs)
     assert P.pkv_get_device_errors() & L.PKV_DEVERR_BLOCK_ID
     assert torch.equal(k, k0)
+
+
+def test_bad_prefix_group_is_flagged_and_skipped():
+    """A group whose members run past the batch is never used: flagged,
+    its sequences decoded as usual."""
+    import workloads as W
+    from tests.gpu_harness import assert_attention_close, compare_step, out_to_double
+    P.pkv_get_device_errors()
+    w = W.shared_prefix(seed=3, prompts=2, samples=4, prefix=64, tail_lo=1, tail_hi=40, H=4,
+                        D=64)
+    r = compare_step(w, partition_tokens=64)
+    st = r["step"]
+    bad = np.array([[0, 4, 64], [6, 4, 64]], dtype=np.int32)  # the second runs past S = 8
+    st.decode_shared_prefix(bad)
+    torch.cuda.synchronize()
+    assert P.pkv_get_device_errors() & L.PKV_DEVERR_GROUP
+    assert_attention_close(out_to_double(st.out), r["ref"].out, "bad group")
