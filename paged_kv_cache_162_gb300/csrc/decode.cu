@@ -32,13 +32,13 @@
 //    workspace; the CTA that finishes a (sequence, head group) last -- known
 //    from an atomic ticket, no waiting -- merges them.  A single-partition
 //    context writes its output directly.
-//  * Scheduling: a one-CTA plan kernel lists the (sequence, partition)
-//    items, full partitions first and partial ones last, and resets the
-//    work counter and tickets.  The decode kernel is persistent (as many
-//    CTAs as fit on the SMs) and takes items from the counter, longest
-//    first, so the tail is at most one partition long.  It is launched with
-//    programmatic dependent launch so its CTAs are resident when the plan
-//    kernel ends.
+//  * Scheduling: a one-CTA plan kernel chooses the partition size, lists the
+//    (sequence, partition) items -- full partitions in sequence order, with
+//    the partial (last) partitions before or after them, see plan_kernel --
+//    and resets the work counter and tickets.  The decode kernel is
+//    persistent (as many CTAs as fit on the SMs) and takes items from the
+//    counter.  It is launched with programmatic dependent launch so its
+//    CTAs are resident when the plan kernel ends.
 //  * Safety: a table entry outside [0, NB) or a context outside
 //    [0, max_context_len] is never dereferenced; the kernel masks it and
 //    sets a bit in the device error word.  No CTA ever waits on another.
@@ -151,8 +151,16 @@ __device__ __forceinline__ int clamp_ctx(int c, int max_ctx) {
 //
 // Partition size when the caller leaves it to the library: the largest of
 // pt_min, 2*pt_min, ... that still gives every resident CTA at least
-// kItemsPerCta items (so the tail is short) and is at most half of the mean
+// kItemsPerCta items (so the tail is short) and is at most 3/4 of the mean
 // context (so ragged contexts split into similar pieces).
+//
+// Order of the items: when the partial (last) partitions are well filled --
+// on average at least 3/8 of a partition -- they go first.  Their spread of
+// lengths staggers the CTAs, so the full partitions that follow do not run
+// in lock-step waves, and each sequence's merge follows its last full
+// partition through the run instead of piling up at the end.  Nearly empty
+// partial partitions go last instead, where they fill the final wave of
+// full ones.  Either way the full partitions keep sequence order.
 __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const int32_t* __restrict__ context_lens,
                                                                 int S, int pt_fixed, int pt_min,
                                                                 int max_ctx, int slots, int HG,
@@ -241,7 +249,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const int32_t* __
             for (int k = 1; k < kAutoCandidates; ++k) {
                 const long long cand = (long long)pt_min << k;
                 grow = grow && (long long)HG * tot[kAutoCandidates + k] >= (long long)kItemsPerCta * slots &&
-                       2 * cand <= mean;
+                       4 * cand <= 3 * mean;
                 if (grow) pick = k;
             }
         }
@@ -283,7 +291,26 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const int32_t* __
         __syncthreads();
     }
 
-    // item list: full partitions first (sequence order), partial ones after
+    // item order: how full are the partial partitions?
+    __shared__ long long s_fill[kWarpsP];
+    __shared__ int s_partials_first;
+    {
+        long long fill = 0;
+        for (int s = tid; s < S; s += kPlanThreads) fill += clamp_ctx(context_lens[s], max_ctx) % PT;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) fill += __shfl_xor_sync(kFull, fill, o);
+        if (lane == 0) s_fill[wid] = fill;
+        __syncthreads();
+        if (tid == 0) {
+            long long f = 0;
+#pragma unroll
+            for (int w = 0; w < kWarpsP; ++w) f += s_fill[w];
+            s_partials_first = 8 * f >= 3 * (long long)(s_items - s_full_total) * PT;
+        }
+        __syncthreads();
+    }
+    const int n_partial = s_items - s_full_total;
+    const bool partials_first = s_partials_first != 0;
     for (int base = 0; base < S; base += kPlanThreads) {
         const int s = base + tid;
         int nf = 0, np = 0, skip = 0;
@@ -304,8 +331,10 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const int32_t* __
         int off_f = carry[0] + a - (nf - skip), off_p = carry[1] + b - np;
         for (int w = 0; w < wid; ++w) { off_f += wsum[0][w]; off_p += wsum[1][w]; }
         if (s < S) {
-            for (int k = skip; k < nf; ++k) ws.items[off_f + k - skip] = (s << 16) | k;
-            if (np) ws.items[s_full_total + off_p] = (s << 16) | nf;
+            const int at_f = partials_first ? n_partial + off_f : off_f;
+            const int at_p = partials_first ? off_p : s_full_total + off_p;
+            for (int k = skip; k < nf; ++k) ws.items[at_f + k - skip] = (s << 16) | k;
+            if (np) ws.items[at_p] = (s << 16) | nf;
             ws.nparts[s] = nf + np;
         }
         __syncthreads();
@@ -542,17 +571,34 @@ __device__ __forceinline__ void attend_partition(const DecodeParams& a, int s, i
 
 // Merge the partitions of one (sequence, head): with M = max_p m_p,
 // out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p.
+// Partitions go in chunks of 32: lane i holds the weight of the chunk's
+// partition i, and the chunk's acc rows are loaded 8 at a time with no
+// dependent load in between.  The sums keep partition order.
 template <class E, int D>
 __device__ __forceinline__ void merge_partitions(const DecodeParams& a, int s, int h, int np,
                                                  int lane) {
     constexpr int DPL = D / 32;  // dims per lane
     const int64_t base = ((int64_t)s * a.H + h) * a.max_parts;
-    float M = -INFINITY;
-    for (int p = lane; p < np; p += 32) M = fmaxf(M, __ldcg(a.ws.m + base + p));
+    const float* accp = a.ws.acc + base * D + lane * DPL;
+    auto load_acc = [&](int p, float (&v)[DPL]) {
+        if constexpr (DPL == 4) {
+            const float4 t = __ldcg(reinterpret_cast<const float4*>(accp + (int64_t)p * D));
+            v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+        } else {
+            const float2 t = __ldcg(reinterpret_cast<const float2*>(accp + (int64_t)p * D));
+            v[0] = t.x; v[1] = t.y;
+        }
+    };
+
+    float m0 = -INFINITY, l0 = 0.f;
+    if (lane < np) { m0 = __ldcg(a.ws.m + base + lane); l0 = __ldcg(a.ws.l + base + lane); }
+    float M = m0;
+    for (int p = lane + 32; p < np; p += 32) M = fmaxf(M, __ldcg(a.ws.m + base + p));
 #pragma unroll
     for (int mask = 16; mask >= 1; mask >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, mask));
-    float L = 0.f;
-    for (int p = lane; p < np; p += 32) {
+    const float w0 = (m0 == -INFINITY) ? 0.f : exp2f(m0 - M);
+    float L = w0 * l0;
+    for (int p = lane + 32; p < np; p += 32) {
         const float mp = __ldcg(a.ws.m + base + p);
         if (mp != -INFINITY) L = fmaf(exp2f(mp - M), __ldcg(a.ws.l + base + p), L);
     }
@@ -562,18 +608,35 @@ __device__ __forceinline__ void merge_partitions(const DecodeParams& a, int s, i
     float o[DPL];
 #pragma unroll
     for (int j = 0; j < DPL; ++j) o[j] = 0.f;
-#pragma unroll 4
-    for (int p = 0; p < np; ++p) {
-        const float mp = __ldcg(a.ws.m + base + p);
-        const float w = (mp == -INFINITY) ? 0.f : exp2f(mp - M);
-        const float* src = a.ws.acc + (base + p) * D + lane * DPL;
-        if constexpr (DPL == 4) {
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
-            o[0] = fmaf(w, v.x, o[0]); o[1] = fmaf(w, v.y, o[1]);
-            o[2] = fmaf(w, v.z, o[2]); o[3] = fmaf(w, v.w, o[3]);
-        } else {
-            const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
-            o[0] = fmaf(w, v.x, o[0]); o[1] = fmaf(w, v.y, o[1]);
+    for (int c0 = 0; c0 < np; c0 += 32) {  // c0 and n are the same in every lane
+        const int n = min(np - c0, 32);
+        float wl = w0;
+        if (c0 > 0) {
+            wl = 0.f;
+            if (lane < n) {
+                const float mp = __ldcg(a.ws.m + base + c0 + lane);
+                if (mp != -INFINITY) wl = exp2f(mp - M);
+            }
+        }
+        for (int p = 0; p < n; p += 8) {
+            float v[8][DPL];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (p + u < n) {
+                    load_acc(c0 + p + u, v[u]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < DPL; ++j) v[u][j] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float w = __shfl_sync(kFull, wl, (p + u) & 31);
+                if (p + u < n) {
+#pragma unroll
+                    for (int j = 0; j < DPL; ++j) o[j] = fmaf(w, v[u][j], o[j]);
+                }
+            }
         }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;

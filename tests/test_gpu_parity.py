@@ -117,15 +117,56 @@ def _chosen_partition(st):
 
 def test_automatic_partition_size_on_full_workloads():
     """The automatic choice (largest of 64, 128, ... tokens giving >= 6 items
-    per resident CTA and <= half the mean context) on GB300's 152 SMs picks
+    per resident CTA and <= 3/4 of the mean context) on GB300's 152 SMs picks
     the sizes measured fastest for these workloads."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     if sms != 152:
         pytest.skip("expected sizes are for a 152-SM GB300")
-    for make, want in ((W.llama7b_batch64, 128), (W.continuous_batching_bf16, 256),
+    for make, want in ((W.llama7b_batch64, 128), (W.continuous_batching_bf16, 512),
                        (W.shared_prefix, 512), (lambda: W.long_context(bs=16), 512)):
         w = make()
         st = device_step(w, 0)
         st.run()
         torch.cuda.synchronize()
         assert _chosen_partition(st) == want, (w.name, _chosen_partition(st))
+
+
+def _item_list(st):
+    # header: n_items at byte 4; the packed (seq << 16 | partition) items
+    # start at byte 256
+    n = int(st.workspace[4:8].view(torch.int32).item())
+    items = st.workspace[256:256 + 4 * n].view(torch.int32).cpu().numpy()
+    return items >> 16, items & 0xFFFF
+
+
+@pytest.mark.parametrize("make,pt", [
+    (lambda: W.small_case(81, S=40, H=8, D=128, ctx_lo=0, ctx_hi=700), 0),
+    (lambda: W.small_case(82, S=40, H=8, D=128, ctx_lo=1, ctx_hi=700), 64),
+    (lambda: W.small_case(83, S=33, H=4, D=64, ctx=[128 * (i % 5) + (i % 3) for i in range(33)]), 128),
+    (W.llama7b_batch64, 0),
+    (lambda: W.shared_prefix(cow=True), 0),
+])
+def test_plan_item_list(make, pt):
+    """The plan lists every (sequence, partition) once; full partitions in
+    sequence order; the partial (last) partitions all before the full ones
+    when they average at least 3/8 of a partition, else all after them."""
+    w = make()
+    st = device_step(w, pt)
+    st.run()
+    torch.cuda.synchronize()
+    PT = _chosen_partition(st)
+    seq, part = _item_list(st)
+    ctx = np.asarray(w.context_lens, dtype=np.int64)
+    want = {(s, k) for s in range(w.S) for k in range(max(1, -(-int(ctx[s]) // PT)))}
+    got = list(zip(seq.tolist(), part.tolist()))
+    assert len(got) == len(set(got)) and set(got) == want
+    is_partial = np.array([(ctx[s] % PT != 0 or ctx[s] == 0) and k == ctx[s] // PT
+                           for s, k in got], dtype=bool)
+    n_partial = int(is_partial.sum())
+    full = [g for g, p in zip(got, is_partial) if not p]
+    assert full == sorted(full)
+    fill = int((ctx % PT).sum())
+    if n_partial:
+        first = 8 * fill >= 3 * n_partial * PT
+        block = is_partial[:n_partial] if first else is_partial[len(got) - n_partial:]
+        assert block.all(), (first, n_partial)
