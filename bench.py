@@ -413,18 +413,13 @@ def run_ours(args):
     dec_ms = kernels["decode"]["ms"]
 
     # ---- end to end: host buffers, copies inside the timed region, one
-    # CUDA graph per step (copies in, the four kernels, copy out), then a sync
-    pin = lambda t: t.cpu().pin_memory()
-    dev_in = {"q": st.q, "new_k": st.new_k, "new_v": st.new_v, "block_tables": st.block_tables,
-              "context_lens": st.context_lens, "seq_idx": st.seq_idx, "pos": st.pos}
-    if has_pairs:
-        dev_in["pairs"] = st.pairs
-    host_in = {k: pin(t) for k, t in dev_in.items()}
+    # CUDA graph per step (one copy of the packed inputs in, the kernels,
+    # copy of the output out), then a sync
+    dev_in, host_in = st.pack_inputs()
     host_out = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    h2d = host_in.numel()
     d2h = host_out.numel() * host_out.element_size()
-    g = StepGraph(st, stream, h2d=[(dev_in[k], host_in[k]) for k in dev_in],
-                  d2h=[(host_out, st.out)])
+    g = StepGraph(st, stream, h2d=[(dev_in, host_in)], d2h=[(host_out, st.out)])
 
     def e2e_step():
         g.replay()          # on `stream`
@@ -492,9 +487,10 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "e2e": {"value": weak_value(kv_bytes, world, e2e_ms), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                    "method": "one CUDA graph per step (H2D copies of the step's inputs from "
-                              "pinned memory, the step's kernels, D2H copy of the output), "
-                              "then a stream sync"},
+                    "method": "one CUDA graph per step (one H2D copy of the step's packed "
+                              "inputs -- q, new K/V, block tables, context lengths, token "
+                              "positions, copy pairs -- from pinned memory, the step's kernels, "
+                              "D2H copy of the output), then a stream sync"},
             "kernels": kernels,
             "gpu_launches": launches_per_step * K,
             "clocks": clocks.summary(),

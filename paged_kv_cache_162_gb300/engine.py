@@ -12,6 +12,7 @@ The step, in the order a serving loop runs it ("3.3 页面级显存管理" 3.3.2
 """
 from __future__ import annotations
 
+import ctypes
 import math
 import time
 
@@ -309,6 +310,35 @@ class DecodeStep:
         self.decode(st)
         return pairs
 
+    def pack_inputs(self):
+        """Move the step's device inputs (q, new K/V, block tables, context
+        lengths, token positions, copy pairs) into one device buffer, at
+        256-byte aligned offsets, so that one copy uploads all of them.
+
+        Returns (device buffer, pinned host buffer holding the same bytes).
+        The step's tensors become views of the device buffer; a caller
+        writes the next step's inputs into the host buffer at the same
+        offsets (`input_offsets`) and copies it over."""
+        if self.block_tables is None:
+            self.plan()
+        names = ["q", "new_k", "new_v", "block_tables", "context_lens", "seq_idx", "pos"]
+        if self.pairs.numel():
+            names.append("pairs")
+        offsets, o = {}, 0
+        for n in names:
+            t = getattr(self, n)
+            offsets[n] = o
+            o = (o + t.numel() * t.element_size() + 255) // 256 * 256
+        buf = torch.empty(max(o, 256), dtype=torch.uint8, device=self.device)
+        for n in names:
+            t = getattr(self, n)
+            nbytes = t.numel() * t.element_size()
+            view = buf[offsets[n]:offsets[n] + nbytes].view(t.dtype).view(t.shape)
+            view.copy_(t)
+            setattr(self, n, view)
+        self.input_offsets = offsets
+        return buf, buf.cpu().pin_memory()
+
     def decode_shared_prefix(self, prefix_groups, stream=None):
         """decode() with the prefix of each group read once (see
         paged_attention_decode_shared_prefix); prefix_groups [G, 3] int32."""
@@ -324,6 +354,20 @@ class DecodeStep:
                                      dtype_code(self.dtype), self.partition_tokens, self.workspace,
                                      self.workspace.numel(), stream)
         return self.out
+
+
+_driver = None
+
+
+def _cu_graph_launch():
+    """The driver's cuGraphLaunch(graph_exec, stream) -> CUresult."""
+    global _driver
+    if _driver is None:
+        lib = ctypes.CDLL("libcuda.so.1")
+        lib.cuGraphLaunch.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+        lib.cuGraphLaunch.restype = ctypes.c_int
+        _driver = lib
+    return _driver.cuGraphLaunch
 
 
 class StepGraph:
@@ -350,8 +394,15 @@ class StepGraph:
             step.run()
             for host, dev in d2h:
                 host.copy_(dev, non_blocking=True)
+        self._exec = ctypes.c_void_p(self.graph.raw_cuda_graph_exec())
+        self._stream = ctypes.c_void_p(stream.cuda_stream)
+        self._launch = _cu_graph_launch()
 
     def replay(self):
-        """Enqueue the captured step on its stream (not torch's current one)."""
-        with torch.cuda.stream(self.stream):
-            self.graph.replay()
+        """Enqueue the captured step on its stream (not torch's current one).
+
+        One driver call: switching torch's current stream around
+        CUDAGraph.replay() costs more host time per step than the launch."""
+        r = self._launch(self._exec, self._stream)
+        if r != 0:
+            raise L.PkvError(L.PKV_ERR_CUDA, f"cuGraphLaunch failed (CUresult {r})")
