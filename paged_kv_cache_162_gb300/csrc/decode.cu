@@ -847,10 +847,16 @@ __device__ __forceinline__ void prefix_partition(const DecodeParams& a, const in
                 Mma<E>::run(sc[1], qa[k], b[2], b[3]);
             }
         }
+        // logits in log2 units, scaled before the max (the scale may be < 0)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[j][e] *= a.qscale;
+        }
         // online softmax per member row (g: [0],[1]; g+8: [2],[3])
         float mt[2];
-        mt[0] = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1])) * a.qscale;
-        mt[1] = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3])) * a.qscale;
+        mt[0] = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+        mt[1] = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             mt[r] = fmaxf(mt[r], __shfl_xor_sync(kFull, mt[r], 1));
@@ -867,10 +873,10 @@ __device__ __forceinline__ void prefix_partition(const DecodeParams& a, const in
         float p[2][4];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            p[j][0] = exp2f(sc[j][0] * a.qscale - mu[0]);
-            p[j][1] = exp2f(sc[j][1] * a.qscale - mu[0]);
-            p[j][2] = exp2f(sc[j][2] * a.qscale - mu[1]);
-            p[j][3] = exp2f(sc[j][3] * a.qscale - mu[1]);
+            p[j][0] = exp2f(sc[j][0] - mu[0]);
+            p[j][1] = exp2f(sc[j][1] - mu[0]);
+            p[j][2] = exp2f(sc[j][2] - mu[1]);
+            p[j][3] = exp2f(sc[j][3] - mu[1]);
         }
         l_run[0] = l_run[0] * corr[0] + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
         l_run[1] = l_run[1] * corr[1] + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);

@@ -57,3 +57,36 @@ def test_shared_prefix_full_workload(cow):
     st.decode_shared_prefix(_groups(w, 8, 1024))
     torch.cuda.synchronize()
     assert_attention_close(out_to_double(st.out), r["ref"].out, "shared prefix full")
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.2])
+def test_zero_and_negative_scale(scale):
+    """The softmax max must be taken after scaling: with a negative scale the
+    largest scaled logit comes from the smallest dot product."""
+    w = W.shared_prefix(seed=11, prompts=2, samples=4, prefix=128, tail_lo=1, tail_hi=60, H=4,
+                        D=128)
+    w.scale = scale
+    r = compare_step(w, partition_tokens=64)
+    st = r["step"]
+    st.out.fill_(float("nan"))
+    st.decode_shared_prefix(_groups(w, 4, 128))
+    torch.cuda.synchronize()
+    assert_attention_close(out_to_double(st.out), r["ref"].out, f"scale {scale}")
+
+
+@pytest.mark.parametrize("bs", [16, 64])
+def test_groups_of_one_with_empty_and_short_contexts(bs):
+    """Groups of one sequence (a sequence always shares its prefix with
+    itself) beside ungrouped sequences, some with empty contexts: the
+    ungrouped and tail items run as groups of one with masked ragged tiles."""
+    ctx = [0, 300, 5, 0, 170, 64, 17, 129]
+    w = W.small_case(seed=bs + 3, S=len(ctx), H=8, D=128, bs=bs, ctx=ctx, n_new=1, NB=80)
+    r = compare_step(w, partition_tokens=64)
+    st = r["step"]
+    st.out.fill_(float("nan"))
+    groups = np.array([[1, 1, 256], [4, 1, 128], [5, 1, 64], [7, 1, 128]], dtype=np.int32)
+    st.decode_shared_prefix(groups)
+    torch.cuda.synchronize()
+    got = out_to_double(st.out)
+    assert_attention_close(got, r["ref"].out, f"groups of one bs{bs}")
+    assert np.all(got[0] == 0.0) and np.all(got[3] == 0.0)
