@@ -202,7 +202,7 @@ def make_workload(name, rank, block_size=0):
 
 
 # --------------------------------------------------------- oracle timing
-def time_oracle(w, seconds_per_step=2.0):
+def time_oracle(w, seconds_per_step=2.0, threads=None):
     """Times one oracle step (slot mapping, cache write, fp64 decode) over a
     bounded sample of the workload: the first n (sequence, head) pairs in
     sequence order, n calibrated so that the step takes about
@@ -213,7 +213,8 @@ def time_oracle(w, seconds_per_step=2.0):
     from oracle import step as OS
     import workloads as W
 
-    threads = K.default_threads()
+    if threads is None:
+        threads = K.default_threads()
     a, tables, nb, pairs = OS.plan(w)
     ids, rob, k_pool, v_pool = OS.build_pool(w, tables, pairs, W.POISON[w.dtype])
     ctx = w.context_lens.astype(np.int64)
@@ -453,12 +454,17 @@ def run_ours(args):
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         dt, sample_bytes, nseq, threads, _ = time_oracle(w)
+        dt1, bytes1, nseq1, _, _ = time_oracle(w, 1.0, threads=1)
         cpu = {"value": sample_bytes / dt / 1e9, "unit": "GB/s", "cores": threads,
                "kind": "oracle",
                "sample": f"one oracle step (slot mapping, cache write, fp64 decode) over the "
                          f"first {int(round(nseq * w.H))} (sequence, head) pairs in sequence "
                          f"order ({nseq:.2f} of {w.S} sequences, "
-                         f"{sample_bytes / 1e6:.1f} MB logical KV), {dt:.2f} s"}
+                         f"{sample_bytes / 1e6:.1f} MB logical KV), {dt:.2f} s",
+               "one_thread": {"value": bytes1 / dt1 / 1e9, "unit": "GB/s", "cores": 1,
+                              "sample": f"the first {int(round(nseq1 * w.H))} (sequence, head) "
+                                        f"pairs, {bytes1 / 1e6:.1f} MB logical KV, "
+                                        f"{dt1:.2f} s"}}
 
     if rank == 0:
         cfg = describe(w)
