@@ -187,7 +187,9 @@ pkv_status pkv_paged_attention_decode_noalloc(
 /* Slot of each new token (address translation, [P3] 3.1.3 steps 1-3):
  *   slot_mapping[t] = block_tables[seq_idx[t]*MB + pos[t]/bs]*bs + pos[t]%bs
  * pos[t] < 0 gives -1 (no write).  A position past the row (pos/bs >= MB)
- * or a seq_idx outside [0, S) gives -1 and sets PKV_DEVERR_POSITION.
+ * or a seq_idx outside [0, S) gives -1 and sets PKV_DEVERR_POSITION; a
+ * position whose table entry is negative (no block mapped) gives -1 and
+ * sets PKV_DEVERR_BLOCK_ID.
  *   slot_mapping  [T] int64 device, written
  *   block_tables  [S][MB] int32 device; seq_idx, pos: [T] int32 device   */
 pkv_status pkv_compute_slot_mapping(int64_t* slot_mapping, const int32_t* block_tables,

@@ -75,7 +75,8 @@ void oracle_slot_mapping(int64_t* slot, const int32_t* block_tables, int MB,
         int64_t logical = pos[t] / block_size;
         int64_t offset = pos[t] % block_size;
         int64_t physical = block_tables[(int64_t)seq_idx[t] * MB + logical];
-        slot[t] = physical * block_size + offset;
+        /* no block mapped at that logical block: no slot to write */
+        slot[t] = physical < 0 ? -1 : physical * block_size + offset;
     }
 }
 

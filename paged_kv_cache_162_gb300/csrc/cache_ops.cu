@@ -40,7 +40,12 @@ __global__ void slot_mapping_kernel(int64_t* __restrict__ slot, const int32_t* _
         slot[t] = -1;
         return;
     }
-    int64_t phys = bt[(int64_t)s * MB + logical];
+    const int64_t phys = bt[(int64_t)s * MB + logical];
+    if (phys < 0) {  // the table has no block there: nothing to write into
+        pkv::report(err, PKV_DEVERR_BLOCK_ID);
+        slot[t] = -1;
+        return;
+    }
     slot[t] = phys * bs + (p - logical * bs);
 }
 

@@ -168,13 +168,15 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const int32_t* __
                                                                 const int32_t* __restrict__ groups,
                                                                 int G, int* err) {
     constexpr int kWarpsP = kPlanThreads / 32;
-    constexpr int kVals = 2 * kAutoCandidates + 1;  // full and all per candidate, sum of contexts
+    constexpr int kVals = 2 * kAutoCandidates;  // full and all partitions per candidate
     // context_lens may come from the kernel before this one
     asm volatile("griddepcontrol.wait;" ::: "memory");
     // the decode kernel may become resident now; it waits for this grid
     asm volatile("griddepcontrol.launch_dependents;");
     __shared__ int red[kWarpsP][kVals];
     __shared__ int tot[kVals];
+    __shared__ long long red_ctx[kWarpsP];
+    __shared__ long long s_ctx_sum;  // may exceed 2^31
     __shared__ int wsum[2][kWarpsP];
     __shared__ int carry[2];
     __shared__ int s_pt, s_full_total, s_items;
@@ -184,6 +186,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const int32_t* __
 
     // per candidate partition size: full partitions and all partitions
     int v[kVals];
+    long long ctx_sum = 0;
 #pragma unroll
     for (int k = 0; k < kVals; ++k) v[k] = 0;
     for (int s = tid; s < S; s += kPlanThreads) {
@@ -192,7 +195,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const int32_t* __
             pkv::report(err, PKV_DEVERR_CONTEXT);
             c = clamp_ctx(c, max_ctx);
         }
-        v[2 * kAutoCandidates] += c;
+        ctx_sum += c;
 #pragma unroll
         for (int k = 0; k < kAutoCandidates; ++k) {
             if (k < ncand) {
@@ -208,9 +211,12 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const int32_t* __
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) v[k] += __shfl_xor_sync(kFull, v[k], o);
     }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) ctx_sum += __shfl_xor_sync(kFull, ctx_sum, o);
     if (lane == 0) {
 #pragma unroll
         for (int k = 0; k < kVals; ++k) red[wid][k] = v[k];
+        red_ctx[wid] = ctx_sum;
     }
     __syncthreads();
     if (tid < kVals) {
@@ -218,6 +224,12 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const int32_t* __
 #pragma unroll
         for (int w = 0; w < kWarpsP; ++w) t += red[w][tid];
         tot[tid] = t;
+    }
+    if (tid == kVals) {
+        long long t = 0;
+#pragma unroll
+        for (int w = 0; w < kWarpsP; ++w) t += red_ctx[w];
+        s_ctx_sum = t;
     }
     __syncthreads();
     // shared prefixes (automatic size): partitions no longer than the
@@ -243,7 +255,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const int32_t* __
                 if (fits) pick = k;
             }
         } else if (!fixed) {
-            const long long mean = S > 0 ? tot[2 * kAutoCandidates] / S : 0;
+            const long long mean = S > 0 ? s_ctx_sum / S : 0;
             bool grow = true;
 #pragma unroll
             for (int k = 1; k < kAutoCandidates; ++k) {

@@ -58,6 +58,12 @@ def test_bad_slot_and_position_and_copy_pair():
                            torch.tensor([40, 1], dtype=torch.int32, device="cuda"), 16)
     assert P.pkv_get_device_errors() & L.PKV_DEVERR_POSITION
     assert out.tolist() == [-1, -1]
+    # a position in a logical block the table has not mapped (-1)
+    bt = torch.tensor([[2, -1]], dtype=torch.int32, device="cuda")
+    E.compute_slot_mapping(out, bt, torch.tensor([0, 0], dtype=torch.int32, device="cuda"),
+                           torch.tensor([5, 17], dtype=torch.int32, device="cuda"), 16)
+    assert P.pkv_get_device_errors() & L.PKV_DEVERR_BLOCK_ID
+    assert out.tolist() == [2 * 16 + 5, -1]
     pairs = torch.tensor([[0, 8]], dtype=torch.int64, device="cuda")
     E.copy_blocks(k, v, pairs)
     assert P.pkv_get_device_errors() & L.PKV_DEVERR_BLOCK_ID

@@ -106,6 +106,14 @@ def test_slot_mapping_negative_position_is_skip():
     assert K.slot_mapping(np.zeros((1, 2), np.int32), [0], [-1], 16)[0] == -1
 
 
+def test_slot_mapping_unmapped_block_is_skip():
+    """A position whose logical block has no physical block (-1 in the
+    table) gets no slot, whatever its offset."""
+    table = np.array([[7, -1]], np.int32)
+    got = K.slot_mapping(table, [0, 0, 0], [3, 16, 31], 16)
+    assert got.tolist() == [7 * 16 + 3, -1, -1]
+
+
 # ----------------------------------------------------------- sizes on pages
 def test_kv_bytes_formula_matches_pages():
     g = _golden("kv_sizes.json")
