@@ -242,8 +242,11 @@ class DecodeStep:
         """One beam-search step after plan(): every sequence b continues from
         sequence parents[b] (fork: share the parent's blocks), appends one
         token (copy-on-write of its shared partial block first), then the
-        device copies, writes and attends.  new_k/new_v/q: [S, H, D] uint16
-        bit patterns.  Returns the (src, dst) copy pairs of the step."""
+        device copies, writes and attends.  new_k/new_v/q: [S, H, D] 16-bit
+        values, either host arrays of uint16 bit patterns (staged and
+        uploaded with the tables) or device tensors (used in place, as a
+        model on the device would produce them).  Returns the (src, dst)
+        copy pairs of the step."""
         S, MB, H, D, bs = self.S, self.MB, self.H, self.D, self.bs
         if not hasattr(self, "beam_ctx"):
             self.beam_ctx = self.context_lens_host.astype(np.int32).copy()
@@ -273,18 +276,21 @@ class DecodeStep:
         i32[S * MB + S:] = ctx
         if P:
             slot["i64"].numpy()[:2 * P] = pairs.ravel()
-        u16 = slot["u16"].numpy().view(np.uint16)
         n = S * H * D
-        u16[:n] = np.asarray(q).ravel()
-        u16[n:2 * n] = np.asarray(new_k).ravel()
-        u16[2 * n:] = np.asarray(new_v).ravel()
+        on_device = all(isinstance(t, torch.Tensor) and t.is_cuda for t in (q, new_k, new_v))
+        if not on_device:
+            u16 = slot["u16"].numpy().view(np.uint16)
+            u16[:n] = np.asarray(q).ravel()
+            u16[n:2 * n] = np.asarray(new_k).ravel()
+            u16[2 * n:] = np.asarray(new_v).ravel()
         st = stream if stream is not None else torch.cuda.current_stream()
         d = self._beam_dev
         with torch.cuda.stream(st):
             d["i32"].copy_(slot["i32"], non_blocking=True)
             if P:
                 d["i64"][:2 * P].copy_(slot["i64"][:2 * P], non_blocking=True)
-            d["u16"].copy_(slot["u16"], non_blocking=True)
+            if not on_device:
+                d["u16"].copy_(slot["u16"], non_blocking=True)
             ev = torch.cuda.Event()
             ev.record(st)
         slot["done"] = ev
@@ -294,10 +300,18 @@ class DecodeStep:
         if getattr(self, "_beam_seq_idx", None) is None:
             self._beam_seq_idx = torch.arange(S, dtype=torch.int32, device=self.device)
         self.seq_idx = self._beam_seq_idx
-        tok = d["u16"].view(self.dtype)
-        self.q = tok[:n].view(S, H, D)
-        self.new_k = tok[n:2 * n].view(S, H, D)
-        self.new_v = tok[2 * n:].view(S, H, D)
+        if on_device:
+            def as_tokens(t):
+                if t.element_size() != 2 or t.numel() != n or not t.is_contiguous():
+                    raise L.PkvError(L.PKV_ERR_INVALID_ARG,
+                                     "beam_step: q/new_k/new_v must be contiguous [S, H, D] 16-bit")
+                return t.view(self.dtype).view(S, H, D)
+            self.q, self.new_k, self.new_v = as_tokens(q), as_tokens(new_k), as_tokens(new_v)
+        else:
+            tok = d["u16"].view(self.dtype)
+            self.q = tok[:n].view(S, H, D)
+            self.new_k = tok[n:2 * n].view(S, H, D)
+            self.new_v = tok[2 * n:].view(S, H, D)
         self.T = S
         need = workspace_size(S, H, D, self.max_context_len, self.partition_tokens)
         if self.workspace.numel() < need:

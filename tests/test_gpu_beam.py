@@ -12,15 +12,22 @@ from tests.gpu_harness import assert_attention_close, device_step
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("bs", [16, 8])
-def test_beam_search_steps_match_oracle(bs):
+@pytest.mark.parametrize("bs,device_tokens", [(16, False), (8, False), (16, True)])
+def test_beam_search_steps_match_oracle(bs, device_tokens):
     bw = W.beam_search(seed=7 + bs, requests=3, beams=4, prompt_lo=20, prompt_hi=70, steps=6,
                        H=4, D=64, bs=bs)
     st = device_step(bw.init, 32)
     st.plan()
+    if device_tokens:
+        # the step's q and new K/V already on the device, as a model makes them
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+        toks = (dev(bw.new_k), dev(bw.new_v), dev(bw.q))
     copies = 0
     for i, (bt, pairs, slots, k_pool, v_pool, ids, out) in enumerate(OS.run_beam(bw, nthreads=2)):
-        got_pairs = st.beam_step(bw.parents[i], bw.new_k[i], bw.new_v[i], bw.q[i])
+        if device_tokens:
+            got_pairs = st.beam_step(bw.parents[i], toks[0][i], toks[1][i], toks[2][i])
+        else:
+            got_pairs = st.beam_step(bw.parents[i], bw.new_k[i], bw.new_v[i], bw.q[i])
         torch.cuda.synchronize()
         assert np.array_equal(st.tables_host, bt), f"step {i}: tables"
         assert np.array_equal(got_pairs, pairs), f"step {i}: pairs"
