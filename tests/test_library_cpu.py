@@ -67,7 +67,12 @@ def _decode_args(**kw):
     (dict(partition_tokens=40), L.PKV_ERR_INVALID_ARG),
     (dict(bs=32, partition_tokens=48), L.PKV_ERR_INVALID_ARG),
     (dict(scale=float("nan")), L.PKV_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), L.PKV_ERR_INVALID_ARG),
     (dict(H=0), L.PKV_ERR_INVALID_ARG),
+    # one past the limits of the packed (sequence << 16 | partition) items
+    (dict(S=32768), L.PKV_ERR_INVALID_ARG),
+    (dict(S=1, MB=65536, bs=64, max_context_len=65536 * 64, partition_tokens=64),
+     L.PKV_ERR_INVALID_ARG),
 ])
 def test_decode_rejects_bad_arguments_before_launch(kw, status):
     a = _decode_args(**kw)
