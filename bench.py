@@ -53,6 +53,8 @@ def parse_args(argv=None):
                    help="llama7b_batch64 only: another block size (8, 16, 32, 64)")
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--unfused", action="store_true",
+                   help="time the step as four separate calls instead of pkv_decode_step")
     p.add_argument("--measure", choices=["step", "swap_blocks", "beam_search"], default="step",
                    help="swap_blocks: GPU <-> pinned-host block copies; beam_search: fork + "
                         "copy-on-write every step")
@@ -318,7 +320,12 @@ def run_ours(args):
     # algorithmic bytes of one decode launch: KV rows + q + out + table entries
     dec_bytes = (kv_bytes + 2 * w.S * w.H * w.D * 2
                  + int(np.ceil(w.context_lens / w.bs).sum()) * 4)
-    launches_per_step = (1 if len(st.pairs_host) else 0) + (2 if w.T else 0) + 2
+    # the step: copy_blocks (if any pairs), then pkv_decode_step (slot
+    # mapping + cache write + plan in one kernel, then decode); --unfused and
+    # shared-prefix decode use the separate calls
+    fused = not (args.unfused or args.shared_prefix)
+    launches_per_step = ((1 if len(st.pairs_host) else 0) +
+                         (2 if fused else (2 if w.T else 0) + 2))
 
     from paged_kv_cache_162_gb300.engine import (StepGraph, compute_slot_mapping, copy_blocks,
                                                  reshape_and_cache)
@@ -339,6 +346,9 @@ def run_ours(args):
             st.scale, st.max_context_len, args.partition_tokens, workspace=ws_sp, stream=stream)
 
     def step():
+        if fused:
+            st.run(stream, fused=True)
+            return
         if has_pairs:
             copy_blocks(st.k_cache, st.v_cache, st.pairs, stream)
         if w.T:
@@ -420,7 +430,7 @@ def run_ours(args):
     host_out = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
     h2d = host_in.numel()
     d2h = host_out.numel() * host_out.element_size()
-    g = StepGraph(st, stream, h2d=[(dev_in, host_in)], d2h=[(host_out, st.out)])
+    g = StepGraph(st, stream, h2d=[(dev_in, host_in)], d2h=[(host_out, st.out)], fused=fused)
 
     def e2e_step():
         g.replay()          # on `stream`
@@ -475,6 +485,9 @@ def run_ours(args):
                     "l2": f"inputs larger than L2: {kv_bytes / 1e9:.2f} GB of KV read per step "
                           f"vs 129 MB L2; no flush",
                     "parallelism": f"replicas{world}" if world > 1 else "single GPU",
+                    "step_calls": ("copy_blocks (if any pairs) + pkv_decode_step" if fused else
+                                   "copy_blocks, compute_slot_mapping, reshape_and_cache, "
+                                   "decode as separate calls"),
                     "global_batch": w.S * world})
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,

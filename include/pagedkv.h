@@ -118,6 +118,33 @@ pkv_status pkv_paged_attention_decode(
     float scale, pkv_dtype dtype, int partition_tokens,
     void* workspace, size_t workspace_bytes, void* stream);
 
+/* One decode step's device work after the host has made room for the new
+ * tokens (and copied any copy-on-write blocks with pkv_copy_blocks): the
+ * new tokens' slots, their K/V written into the caches, then decode
+ * attention over every sequence's whole context.  The result is exactly
+ * that of pkv_compute_slot_mapping, pkv_reshape_and_cache and
+ * pkv_paged_attention_decode called in that order with the same arguments
+ * (same slots, same cache contents, bit-identical output); it runs in two
+ * kernels instead of four, the slot mapping, cache write and the decode's
+ * work plan in one.  This fusion is this library's; the pages describe the
+ * three operations, not a combined call.
+ *
+ *   key, value    [T][H][D] dtype: K and V of the new tokens, 16-byte aligned
+ *   seq_idx, pos  [T] int32: each new token's sequence and position
+ *   slot_mapping  [T] int64, written: the slots, as pkv_compute_slot_mapping
+ *                 gives them (-1: not written, see there)
+ *   k_cache, v_cache  written for the new tokens, then read
+ *   other arguments as in pkv_paged_attention_decode; context_lens count the
+ *   new tokens.  T = 0 is a plain decode; S = 0 with T > 0 is
+ *   PKV_ERR_INVALID_ARG. */
+pkv_status pkv_decode_step(
+    void* out, const void* q, const void* key, const void* value,
+    void* k_cache, void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, const int32_t* seq_idx, const int32_t* pos,
+    int64_t* slot_mapping, int T, int S, int H, int D, int bs, int NB, int MB,
+    int max_context_len, float scale, pkv_dtype dtype, int partition_tokens,
+    void* workspace, size_t workspace_bytes, void* stream);
+
 /* Decode attention where groups of sequences share a prefix (parallel
  * sampling, beam search, a common system prompt: [P1] 3.3.2 "Copy-on-Write
  * 页面共享机制", [P3] 3.1.5, [P4] "Memory Sharing与写时复制").  Computes exactly

@@ -17,7 +17,7 @@ namespace {
 
 // Address translation of "3.1 PagedAttention的核心原理" 3.1.3 steps 1-3:
 // logical block = pos / bs, offset = pos % bs, physical = table[logical];
-// the slot is the token's row physical*bs + offset.
+// the slot is the token's row physical*bs + offset (pkv::slot_of).
 __global__ void slot_mapping_kernel(int64_t* __restrict__ slot, const int32_t* __restrict__ bt,
                                     const int32_t* __restrict__ seq_idx,
                                     const int32_t* __restrict__ pos, int T, int S, int MB, int bs,
@@ -28,25 +28,7 @@ __global__ void slot_mapping_kernel(int64_t* __restrict__ slot, const int32_t* _
     asm volatile("griddepcontrol.launch_dependents;");
     int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= T) return;
-    int p = pos[t];
-    int s = seq_idx[t];
-    if (p < 0) {
-        slot[t] = -1;
-        return;
-    }
-    int logical = p / bs;
-    if (logical >= MB || s < 0 || s >= S) {
-        pkv::report(err, PKV_DEVERR_POSITION);
-        slot[t] = -1;
-        return;
-    }
-    const int64_t phys = bt[(int64_t)s * MB + logical];
-    if (phys < 0) {  // the table has no block there: nothing to write into
-        pkv::report(err, PKV_DEVERR_BLOCK_ID);
-        slot[t] = -1;
-        return;
-    }
-    slot[t] = phys * bs + (p - logical * bs);
+    slot[t] = pkv::slot_of(bt, seq_idx[t], pos[t], S, MB, bs, err);
 }
 
 // One CTA per new token: copy its H*D-element K row and V row into the
@@ -66,16 +48,7 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
         if (threadIdx.x == 0) pkv::report(err, PKV_DEVERR_SLOT);
         return;
     }
-    const uint4* ks = key + (int64_t)t * vec_per_row;
-    const uint4* vs = value + (int64_t)t * vec_per_row;
-    uint4* kd = k_cache + slot * vec_per_row;
-    uint4* vd = v_cache + slot * vec_per_row;
-    for (int i = threadIdx.x; i < vec_per_row; i += blockDim.x) {
-        uint4 a = ks[i];
-        uint4 b = vs[i];
-        kd[i] = a;
-        vd[i] = b;
-    }
+    pkv::write_token_rows(key, value, k_cache, v_cache, t, slot, vec_per_row);
 }
 
 // Grid (P, splits): CTA (p, y) copies the y-th 1/splits of pair p's K block

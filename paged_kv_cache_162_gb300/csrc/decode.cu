@@ -161,18 +161,28 @@ __device__ __forceinline__ int clamp_ctx(int c, int max_ctx) {
 // partition through the run instead of piling up at the end.  Nearly empty
 // partial partitions go last instead, where they fill the final wave of
 // full ones.  Either way the full partitions keep sequence order.
-__global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const int32_t* __restrict__ context_lens,
-                                                                int S, int pt_fixed, int pt_min,
-                                                                int max_ctx, int slots, int HG,
-                                                                int n_tickets, Workspace ws,
-                                                                const int32_t* __restrict__ groups,
-                                                                int G, int* err) {
+struct PlanArgs {
+    const int32_t* context_lens;
+    int S, pt_fixed, pt_min, max_ctx;
+    int slots;      // CTAs of the decode kernel's grid
+    int HG;         // head groups of 4 heads
+    int n_tickets;  // S * HG
+    Workspace ws;
+    const int32_t* groups;  // shared-prefix groups (G of them) or nullptr
+    int G;
+    int* err;
+};
+
+// The plan, computed by one CTA of kPlanThreads threads.
+__device__ __forceinline__ void plan_cta(const PlanArgs& pa) {
+    const int32_t* __restrict__ context_lens = pa.context_lens;
+    const int S = pa.S, pt_fixed = pa.pt_fixed, pt_min = pa.pt_min, max_ctx = pa.max_ctx;
+    const int slots = pa.slots, HG = pa.HG, n_tickets = pa.n_tickets, G = pa.G;
+    const Workspace& ws = pa.ws;
+    const int32_t* __restrict__ groups = pa.groups;
+    int* err = pa.err;
     constexpr int kWarpsP = kPlanThreads / 32;
     constexpr int kVals = 2 * kAutoCandidates;  // full and all partitions per candidate
-    // context_lens may come from the kernel before this one
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    // the decode kernel may become resident now; it waits for this grid
-    asm volatile("griddepcontrol.launch_dependents;");
     __shared__ int red[kWarpsP][kVals];
     __shared__ int tot[kVals];
     __shared__ long long red_ctx[kWarpsP];
@@ -360,6 +370,89 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const int32_t* __
         *ws.pt = PT;
         *ws.pcounter = 0u;
         *ws.n_pitems = G > 0 ? s_pitems : 0;
+    }
+}
+
+__global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanArgs pa) {
+    // context_lens may come from the kernel before this one
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the decode kernel may become resident now; it waits for this grid
+    asm volatile("griddepcontrol.launch_dependents;");
+    plan_cta(pa);
+}
+
+// The new tokens of one decode step (pkv_decode_step).
+struct TokenArgs {
+    const uint4* key;    // [T][H*D/8]
+    const uint4* value;
+    uint4* k_cache;      // [NB*bs][H*D/8]
+    uint4* v_cache;
+    const int32_t* block_tables;  // [S][MB]
+    const int32_t* seq_idx;  // [T]
+    const int32_t* pos;      // [T]
+    int64_t* slot_mapping;   // [T], written
+    int T, MB, bs, vec_per_row;
+    int64_t num_slots;       // NB * bs
+};
+
+// Prologue of a fused step: CTA 0 plans the decode while the other CTAs
+// each take kPrologueTokens new tokens: their slots (address translation,
+// written out to slot_mapping) and the copies of their K and V rows into
+// the caches -- the work of the slot-mapping, cache-write and plan kernels
+// in one launch.  The plan's registers hold this kernel to 4 CTAs per SM,
+// so each thread keeps the loads of several tokens in flight.
+constexpr int kPrologueTokens = 4;
+
+__global__ void __launch_bounds__(kPlanThreads, 4) step_prologue_kernel(PlanArgs pa, TokenArgs ta) {
+    // inputs may come from the kernel before this one
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the decode kernel may become resident now; it waits for this grid
+    asm volatile("griddepcontrol.launch_dependents;");
+    if (blockIdx.x == 0) {
+        plan_cta(pa);
+        return;
+    }
+    const int t0 = (blockIdx.x - 1) * kPrologueTokens;
+    __shared__ long long s_slot[kPrologueTokens];
+    if (threadIdx.x < kPrologueTokens) {
+        const int t = t0 + threadIdx.x;
+        int64_t slot = -1;
+        if (t < ta.T) {
+            slot = pkv::slot_of(ta.block_tables, ta.seq_idx[t], ta.pos[t], pa.S, ta.MB, ta.bs,
+                                pa.err);
+            ta.slot_mapping[t] = slot;
+            if (slot >= ta.num_slots) {
+                pkv::report(pa.err, PKV_DEVERR_SLOT);
+                slot = -1;
+            }
+        }
+        s_slot[threadIdx.x] = slot;
+    }
+    __syncthreads();
+    const int vpr = ta.vec_per_row;
+    const uint4* __restrict__ key = ta.key + (int64_t)t0 * vpr;
+    const uint4* __restrict__ value = ta.value + (int64_t)t0 * vpr;
+    uint4* __restrict__ kc = ta.k_cache;
+    uint4* __restrict__ vc = ta.v_cache;
+    int64_t slot[kPrologueTokens];
+#pragma unroll
+    for (int j = 0; j < kPrologueTokens; ++j) slot[j] = s_slot[j];
+    for (int i = threadIdx.x; i < vpr; i += blockDim.x) {
+        uint4 kv[kPrologueTokens], vv[kPrologueTokens];
+#pragma unroll
+        for (int j = 0; j < kPrologueTokens; ++j) {
+            if (slot[j] >= 0) {
+                kv[j] = key[(int64_t)j * vpr + i];
+                vv[j] = value[(int64_t)j * vpr + i];
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kPrologueTokens; ++j) {
+            if (slot[j] >= 0) {
+                kc[slot[j] * vpr + i] = kv[j];
+                vc[slot[j] * vpr + i] = vv[j];
+            }
+        }
     }
 }
 
@@ -1174,11 +1267,14 @@ cudaLaunchAttribute pdl_attr() {
     return a;
 }
 
+// Launches the plan (or, with `tokens`, the fused step prologue), then the
+// prefix kernel (with groups) or the decode kernel.
 pkv_status launch_decode(const char* who, const CallShape& cs, void* out, const void* q,
                          const void* k_cache, const void* v_cache, const int32_t* block_tables,
                          const int32_t* context_lens, int S, int H, int D, int bs, int NB, int MB,
                          float scale, pkv_dtype dtype, void* workspace, cudaStream_t st,
-                         const int32_t* groups = nullptr, int G = 0) {
+                         const int32_t* groups = nullptr, int G = 0,
+                         const TokenArgs* tokens = nullptr) {
     DecodeParams p;
     p.out = out;
     p.q = q;
@@ -1210,8 +1306,26 @@ pkv_status launch_decode(const char* who, const CallShape& cs, void* out, const 
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, plan_kernel, context_lens, S, cs.pt_fixed, cs.pt_min,
-                                       cs.max_ctx, grid, p.HG, S * H, p.ws, groups, G, p.err);
+    PlanArgs pa;
+    pa.context_lens = context_lens;
+    pa.S = S;
+    pa.pt_fixed = cs.pt_fixed;
+    pa.pt_min = cs.pt_min;
+    pa.max_ctx = cs.max_ctx;
+    pa.slots = grid;
+    pa.HG = p.HG;
+    pa.n_tickets = S * p.HG;
+    pa.ws = p.ws;
+    pa.groups = groups;
+    pa.G = G;
+    pa.err = p.err;
+    cudaError_t e;
+    if (tokens) {
+        cfg.gridDim = dim3(1 + (unsigned)((tokens->T + kPrologueTokens - 1) / kPrologueTokens));
+        e = cudaLaunchKernelEx(&cfg, step_prologue_kernel, pa, *tokens);
+    } else {
+        e = cudaLaunchKernelEx(&cfg, plan_kernel, pa);
+    }
     if (e != cudaSuccess) {
         snprintf(msg, sizeof msg, "%s plan launch", who);
         return pkv::cuda_fail(e, msg);
@@ -1283,6 +1397,52 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_ca
         return pkv::fail(PKV_ERR_WORKSPACE, "paged_attention_decode: workspace too small");
     return launch_decode(who, cs, out, q, k_cache, v_cache, block_tables, context_lens, S, H, D, bs,
                          NB, MB, scale, dtype, workspace, pkv::as_stream(stream));
+}
+
+pkv_status pkv_decode_step(void* out, const void* q, const void* key, const void* value,
+                           void* k_cache, void* v_cache, const int32_t* block_tables,
+                           const int32_t* context_lens, const int32_t* seq_idx, const int32_t* pos,
+                           int64_t* slot_mapping, int T, int S, int H, int D, int bs, int NB,
+                           int MB, int max_context_len, float scale, pkv_dtype dtype,
+                           int partition_tokens, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+    static const char* who = "decode_step";
+    pkv::clear_error();
+    if (T < 0 || T == INT32_MAX) return pkv::fail(PKV_ERR_INVALID_ARG, "decode_step: bad token count");
+    if (T > 0 && (!key || !value || !seq_idx || !pos || !slot_mapping))
+        return pkv::fail(PKV_ERR_INVALID_ARG, "decode_step: null token pointer");
+    if (T > 0 && (!pkv::aligned16(key) || !pkv::aligned16(value)))
+        return pkv::fail(PKV_ERR_INVALID_ARG, "decode_step: key/value must be 16-byte aligned");
+    if (S > 0 && workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return pkv::fail(PKV_ERR_INVALID_ARG, "decode_step: workspace must be 256-byte aligned");
+    CallShape cs;
+    pkv_status st = check_call(who, out, q, k_cache, v_cache, block_tables, context_lens, S, H, D,
+                               bs, NB, MB, max_context_len, scale, dtype, partition_tokens,
+                               SIZE_MAX, &cs);
+    if (st != PKV_OK) return st;
+    if (S == 0) {
+        if (T == 0) return PKV_OK;
+        return pkv::fail(PKV_ERR_INVALID_ARG, "decode_step: new tokens for an empty batch");
+    }
+    if (!workspace) return pkv::fail(PKV_ERR_INVALID_ARG, "decode_step: null workspace");
+    if (workspace_bytes < cs.L.total)
+        return pkv::fail(PKV_ERR_WORKSPACE, "decode_step: workspace too small");
+    TokenArgs ta;
+    ta.key = static_cast<const uint4*>(key);
+    ta.value = static_cast<const uint4*>(value);
+    ta.k_cache = static_cast<uint4*>(k_cache);
+    ta.v_cache = static_cast<uint4*>(v_cache);
+    ta.block_tables = block_tables;
+    ta.seq_idx = seq_idx;
+    ta.pos = pos;
+    ta.slot_mapping = slot_mapping;
+    ta.T = T;
+    ta.MB = MB;
+    ta.bs = bs;
+    ta.vec_per_row = H * D / 8;
+    ta.num_slots = (int64_t)NB * bs;
+    return launch_decode(who, cs, out, q, k_cache, v_cache, block_tables, context_lens, S, H, D, bs,
+                         NB, MB, scale, dtype, workspace, pkv::as_stream(stream), nullptr, 0, &ta);
 }
 
 size_t pkv_decode_shared_prefix_workspace_size(int S, int H, int D, int G, int max_context_len,

@@ -82,4 +82,50 @@ __device__ __forceinline__ void report(int* err, int bits) {
     if (err) atomicOr(err, bits);
 }
 
+// Slot of the token at position p of sequence s: logical block p / bs,
+// offset p % bs, physical block from the sequence's table row.  -1 means
+// "no write": p < 0; a position past the row or a sequence outside [0, S)
+// (PKV_DEVERR_POSITION); a logical block the table has not mapped
+// (PKV_DEVERR_BLOCK_ID).
+__device__ __forceinline__ int64_t slot_of(const int32_t* __restrict__ bt, int s, int p, int S,
+                                           int MB, int bs, int* err) {
+    if (p < 0) return -1;
+    const int logical = p / bs;
+    if (logical >= MB || s < 0 || s >= S) {
+        report(err, PKV_DEVERR_POSITION);
+        return -1;
+    }
+    const int64_t phys = bt[(int64_t)s * MB + logical];
+    if (phys < 0) {
+        report(err, PKV_DEVERR_BLOCK_ID);
+        return -1;
+    }
+    return phys * bs + (p - logical * bs);
+}
+
+// One CTA copies new token t's K and V rows (vec_per_row 16-byte vectors
+// each) into row `slot` of the caches, two vectors of each in flight per
+// thread.  slot must be in range.
+__device__ __forceinline__ void write_token_rows(const uint4* __restrict__ key,
+                                                 const uint4* __restrict__ value,
+                                                 uint4* __restrict__ k_cache,
+                                                 uint4* __restrict__ v_cache, int t, int64_t slot,
+                                                 int vec_per_row) {
+    const uint4* ks = key + (int64_t)t * vec_per_row;
+    const uint4* vs = value + (int64_t)t * vec_per_row;
+    uint4* kd = k_cache + slot * vec_per_row;
+    uint4* vd = v_cache + slot * vec_per_row;
+    const int step = blockDim.x;
+    int i = threadIdx.x;
+    for (; i + step < vec_per_row; i += 2 * step) {
+        const uint4 a0 = ks[i], a1 = ks[i + step], b0 = vs[i], b1 = vs[i + step];
+        kd[i] = a0; kd[i + step] = a1; vd[i] = b0; vd[i + step] = b1;
+    }
+    if (i < vec_per_row) {
+        const uint4 a = ks[i], b = vs[i];
+        kd[i] = a;
+        vd[i] = b;
+    }
+}
+
 }  // namespace pkv

@@ -68,6 +68,28 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
     return out
 
 
+def decode_step(out, q, key, value, k_cache, v_cache, block_tables, context_lens, seq_idx, pos,
+                slot_mapping, scale=None, max_context_len=0, partition_tokens=0, workspace=None,
+                stream=None):
+    """compute_slot_mapping + reshape_and_cache + paged_attention_decode in
+    two kernels (see pkv_decode_step): the new tokens (key/value [T, H, D],
+    seq_idx/pos [T] int32) are written into the caches, slot_mapping [T]
+    int64 receives their slots, then out = attention over every context."""
+    S, H, D = q.shape
+    NB, bs = k_cache.shape[0], k_cache.shape[1]
+    MB = block_tables.shape[1]
+    T = int(seq_idx.numel())
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if workspace is None:
+        workspace = new_workspace(S, H, D, max_context_len or MB * bs, partition_tokens,
+                                  q.device)
+    L.pkv_decode_step(out, q, key, value, k_cache, v_cache, block_tables, context_lens, seq_idx,
+                      pos, slot_mapping, T, S, H, D, bs, NB, MB, max_context_len, scale,
+                      dtype_code(q.dtype), partition_tokens, workspace, workspace.numel(), stream)
+    return out
+
+
 def paged_attention_decode_shared_prefix(out, q, k_cache, v_cache, block_tables, context_lens,
                                          prefix_groups, scale=None, max_context_len=0,
                                          partition_tokens=0, workspace=None, stream=None):
@@ -198,10 +220,22 @@ class DecodeStep:
         self.pairs = torch.from_numpy(np.ascontiguousarray(pairs)).to(self.device)
         return tables, nb, pairs
 
-    def run(self, stream=None, attention=True, write=True):
-        """The device part of the step (all four kernels)."""
+    def run(self, stream=None, attention=True, write=True, fused=False):
+        """The device part of the step: copy_blocks, slot mapping, cache
+        write, decode.  fused=True runs the last three as pkv_decode_step
+        (two kernels instead of four, the same results)."""
         if self.block_tables is None:
             self.plan()
+        if fused and write and attention:
+            if self.pairs.shape[0]:
+                copy_blocks(self.k_cache, self.v_cache, self.pairs, stream)
+            L.pkv_decode_step(self.out, self.q, self.new_k, self.new_v, self.k_cache, self.v_cache,
+                              self.block_tables, self.context_lens, self.seq_idx, self.pos,
+                              self.slot_mapping, self.T, self.S, self.H, self.D, self.bs, self.NB,
+                              self.MB, self.max_context_len, self.scale, dtype_code(self.dtype),
+                              self.partition_tokens, self.workspace, self.workspace.numel(),
+                              stream)
+            return self.out
         if write:
             if self.pairs.shape[0]:
                 copy_blocks(self.k_cache, self.v_cache, self.pairs, stream)
@@ -389,23 +423,24 @@ class StepGraph:
     of its inputs from pinned host memory and of its output back to it.
 
     h2d: [(device_tensor, pinned_host_tensor), ...] copied in first;
-    d2h: [(pinned_host_tensor, device_tensor), ...] copied out last.
+    d2h: [(pinned_host_tensor, device_tensor), ...] copied out last;
+    fused: run the step through pkv_decode_step (DecodeStep.run).
     The step runs once eagerly before capture so that every per-device
     set-up of the library happens outside the capture.  replay() enqueues
     the whole step on the capture stream with one launch.
     """
 
-    def __init__(self, step: DecodeStep, stream: torch.cuda.Stream, h2d=(), d2h=()):
+    def __init__(self, step: DecodeStep, stream: torch.cuda.Stream, h2d=(), d2h=(), fused=False):
         self.step = step
         self.stream = stream
         with torch.cuda.stream(stream):
-            step.run()
+            step.run(fused=fused)
         stream.synchronize()
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph, stream=stream):
             for dev, host in h2d:
                 dev.copy_(host, non_blocking=True)
-            step.run()
+            step.run(fused=fused)
             for host, dev in d2h:
                 host.copy_(dev, non_blocking=True)
         self._exec = ctypes.c_void_p(self.graph.raw_cuda_graph_exec())

@@ -48,15 +48,16 @@ def assert_attention_close(got: np.ndarray, ref: np.ndarray, what=""):
 
 
 def compare_step(w: W.Workload, partition_tokens=0, items=None, check_caches=True,
-                 nthreads=None):
-    """Full comparison of one step; returns a dict of measured errors."""
+                 nthreads=None, fused=False):
+    """Full comparison of one step; returns a dict of measured errors.
+    fused=True runs the device part through pkv_decode_step."""
     ref = OS.run(w, items=items, nthreads=nthreads)
     st = device_step(w, partition_tokens)
     tables, nb, pairs = st.plan()
     assert np.array_equal(tables, ref.tables), "block tables differ"
     assert np.array_equal(nb, ref.nblocks)
     assert np.array_equal(pairs, ref.pairs), "copy-on-write pairs differ"
-    st.run()
+    st.run(fused=fused)
     torch.cuda.synchronize()
     if w.T:
         slots = st.slot_mapping[:w.T].cpu().numpy()
