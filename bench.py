@@ -323,9 +323,10 @@ def run_ours(args):
     # the step: copy_blocks (if any pairs), then pkv_decode_step (slot
     # mapping + cache write + plan in one kernel, then decode); --unfused and
     # shared-prefix decode use the separate calls
-    fused = not (args.unfused or args.shared_prefix)
+    fused = not args.unfused
+    decode_kernels = 3 if args.shared_prefix else 2   # plan or prologue, [prefix,] decode
     launches_per_step = ((1 if len(st.pairs_host) else 0) +
-                         (2 if fused else (2 if w.T else 0) + 2))
+                         (decode_kernels if fused else (2 if w.T else 0) + decode_kernels))
 
     from paged_kv_cache_162_gb300.engine import (StepGraph, compute_slot_mapping, copy_blocks,
                                                  reshape_and_cache)
@@ -344,6 +345,7 @@ def run_ours(args):
         st.decode = lambda stream=None: paged_attention_decode_shared_prefix(
             st.out, st.q, st.k_cache, st.v_cache, st.block_tables, st.context_lens, groups,
             st.scale, st.max_context_len, args.partition_tokens, workspace=ws_sp, stream=stream)
+        st.prefix_groups, st.workspace = groups, ws_sp   # for the fused step
 
     def step():
         if fused:
@@ -485,7 +487,9 @@ def run_ours(args):
                     "l2": f"inputs larger than L2: {kv_bytes / 1e9:.2f} GB of KV read per step "
                           f"vs 129 MB L2; no flush",
                     "parallelism": f"replicas{world}" if world > 1 else "single GPU",
-                    "step_calls": ("copy_blocks (if any pairs) + pkv_decode_step" if fused else
+                    "step_calls": ("copy_blocks (if any pairs) + pkv_decode_step"
+                                   + (" with prefix groups" if args.shared_prefix else "")
+                                   if fused else
                                    "copy_blocks, compute_slot_mapping, reshape_and_cache, "
                                    "decode as separate calls"),
                     "global_batch": w.S * world})

@@ -125,7 +125,7 @@ pkv_status pkv_paged_attention_decode(
  * that of pkv_compute_slot_mapping, pkv_reshape_and_cache and
  * pkv_paged_attention_decode called in that order with the same arguments
  * (same slots, same cache contents, bit-identical output); it runs in two
- * kernels instead of four, the slot mapping, cache write and the decode's
+ * kernels instead of four (three with prefix groups), the slot mapping, cache write and the decode's
  * work plan in one.  This fusion is this library's; the pages describe the
  * three operations, not a combined call.
  *
@@ -134,6 +134,11 @@ pkv_status pkv_paged_attention_decode(
  *   slot_mapping  [T] int64, written: the slots, as pkv_compute_slot_mapping
  *                 gives them (-1: not written, see there)
  *   k_cache, v_cache  written for the new tokens, then read
+ *   prefix_groups, G  G = 0 (prefix_groups may be NULL): the decode is
+ *                 pkv_paged_attention_decode's.  G > 0: it is
+ *                 pkv_paged_attention_decode_shared_prefix's with these
+ *                 groups, and the workspace is sized by
+ *                 pkv_decode_shared_prefix_workspace_size.
  *   other arguments as in pkv_paged_attention_decode; context_lens count the
  *   new tokens.  T = 0 is a plain decode; S = 0 with T > 0 is
  *   PKV_ERR_INVALID_ARG. */
@@ -141,9 +146,10 @@ pkv_status pkv_decode_step(
     void* out, const void* q, const void* key, const void* value,
     void* k_cache, void* v_cache, const int32_t* block_tables,
     const int32_t* context_lens, const int32_t* seq_idx, const int32_t* pos,
-    int64_t* slot_mapping, int T, int S, int H, int D, int bs, int NB, int MB,
-    int max_context_len, float scale, pkv_dtype dtype, int partition_tokens,
-    void* workspace, size_t workspace_bytes, void* stream);
+    int64_t* slot_mapping, const int32_t* prefix_groups, int G, int T, int S,
+    int H, int D, int bs, int NB, int MB, int max_context_len, float scale,
+    pkv_dtype dtype, int partition_tokens, void* workspace,
+    size_t workspace_bytes, void* stream);
 
 /* Decode attention where groups of sequences share a prefix (parallel
  * sampling, beam search, a common system prompt: [P1] 3.3.2 "Copy-on-Write

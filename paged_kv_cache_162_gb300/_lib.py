@@ -59,8 +59,8 @@ SIGNATURES = {
     "pkv_decode_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "pkv_paged_attention_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
                                         _I, _P, _SZ, _P]),
-    "pkv_decode_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
-                             _I, _I, _F, _I, _I, _P, _SZ, _P]),
+    "pkv_decode_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                             _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P]),
     "pkv_decode_shared_prefix_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "pkv_paged_attention_decode_shared_prefix": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
                                                       _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P]),
@@ -160,13 +160,13 @@ def pkv_paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_l
 
 
 def pkv_decode_step(out, q, key, value, k_cache, v_cache, block_tables, context_lens, seq_idx, pos,
-                    slot_mapping, T, S, H, D, bs, NB, MB, max_context_len, scale, dtype,
-                    partition_tokens, workspace, workspace_bytes, stream=None) -> None:
+                    slot_mapping, prefix_groups, G, T, S, H, D, bs, NB, MB, max_context_len, scale,
+                    dtype, partition_tokens, workspace, workspace_bytes, stream=None) -> None:
     check(lib().pkv_decode_step(
         ptr(out), ptr(q), ptr(key), ptr(value), ptr(k_cache), ptr(v_cache), ptr(block_tables),
-        ptr(context_lens), ptr(seq_idx), ptr(pos), ptr(slot_mapping), T, S, H, D, bs, NB, MB,
-        max_context_len, float(scale), int(dtype), partition_tokens, ptr(workspace),
-        int(workspace_bytes), stream_handle(stream)), "decode_step")
+        ptr(context_lens), ptr(seq_idx), ptr(pos), ptr(slot_mapping), ptr(prefix_groups), G, T, S,
+        H, D, bs, NB, MB, max_context_len, float(scale), int(dtype), partition_tokens,
+        ptr(workspace), int(workspace_bytes), stream_handle(stream)), "decode_step")
 
 
 def pkv_decode_shared_prefix_workspace_size(S, H, D, G, max_context_len, partition_tokens=0):

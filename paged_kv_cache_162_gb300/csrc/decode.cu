@@ -1402,13 +1402,15 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_ca
 pkv_status pkv_decode_step(void* out, const void* q, const void* key, const void* value,
                            void* k_cache, void* v_cache, const int32_t* block_tables,
                            const int32_t* context_lens, const int32_t* seq_idx, const int32_t* pos,
-                           int64_t* slot_mapping, int T, int S, int H, int D, int bs, int NB,
-                           int MB, int max_context_len, float scale, pkv_dtype dtype,
-                           int partition_tokens, void* workspace, size_t workspace_bytes,
-                           void* stream) {
+                           int64_t* slot_mapping, const int32_t* prefix_groups, int G, int T,
+                           int S, int H, int D, int bs, int NB, int MB, int max_context_len,
+                           float scale, pkv_dtype dtype, int partition_tokens, void* workspace,
+                           size_t workspace_bytes, void* stream) {
     static const char* who = "decode_step";
     pkv::clear_error();
     if (T < 0 || T == INT32_MAX) return pkv::fail(PKV_ERR_INVALID_ARG, "decode_step: bad token count");
+    if (G < 0 || G > 32767 || (G > 0 && !prefix_groups))
+        return pkv::fail(PKV_ERR_INVALID_ARG, "decode_step: bad groups");
     if (T > 0 && (!key || !value || !seq_idx || !pos || !slot_mapping))
         return pkv::fail(PKV_ERR_INVALID_ARG, "decode_step: null token pointer");
     if (T > 0 && (!pkv::aligned16(key) || !pkv::aligned16(value)))
@@ -1424,6 +1426,7 @@ pkv_status pkv_decode_step(void* out, const void* q, const void* key, const void
         if (T == 0) return PKV_OK;
         return pkv::fail(PKV_ERR_INVALID_ARG, "decode_step: new tokens for an empty batch");
     }
+    if (G > 0) cs.L = layout_shared(S, H, D, G, cs.max_parts);
     if (!workspace) return pkv::fail(PKV_ERR_INVALID_ARG, "decode_step: null workspace");
     if (workspace_bytes < cs.L.total)
         return pkv::fail(PKV_ERR_WORKSPACE, "decode_step: workspace too small");
@@ -1442,7 +1445,8 @@ pkv_status pkv_decode_step(void* out, const void* q, const void* key, const void
     ta.vec_per_row = H * D / 8;
     ta.num_slots = (int64_t)NB * bs;
     return launch_decode(who, cs, out, q, k_cache, v_cache, block_tables, context_lens, S, H, D, bs,
-                         NB, MB, scale, dtype, workspace, pkv::as_stream(stream), nullptr, 0, &ta);
+                         NB, MB, scale, dtype, workspace, pkv::as_stream(stream),
+                         G > 0 ? prefix_groups : nullptr, G, &ta);
 }
 
 size_t pkv_decode_shared_prefix_workspace_size(int S, int H, int D, int G, int max_context_len,

@@ -69,24 +69,29 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
 
 
 def decode_step(out, q, key, value, k_cache, v_cache, block_tables, context_lens, seq_idx, pos,
-                slot_mapping, scale=None, max_context_len=0, partition_tokens=0, workspace=None,
-                stream=None):
-    """compute_slot_mapping + reshape_and_cache + paged_attention_decode in
-    two kernels (see pkv_decode_step): the new tokens (key/value [T, H, D],
+                slot_mapping, prefix_groups=None, scale=None, max_context_len=0,
+                partition_tokens=0, workspace=None, stream=None):
+    """compute_slot_mapping + reshape_and_cache + paged_attention_decode (or
+    its shared-prefix form, with prefix_groups [G, 3] int32 on the device) in
+    fewer kernels (see pkv_decode_step): the new tokens (key/value [T, H, D],
     seq_idx/pos [T] int32) are written into the caches, slot_mapping [T]
     int64 receives their slots, then out = attention over every context."""
     S, H, D = q.shape
     NB, bs = k_cache.shape[0], k_cache.shape[1]
     MB = block_tables.shape[1]
     T = int(seq_idx.numel())
+    G = 0 if prefix_groups is None else int(prefix_groups.shape[0])
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if workspace is None:
-        workspace = new_workspace(S, H, D, max_context_len or MB * bs, partition_tokens,
-                                  q.device)
+        mc = max_context_len or MB * bs
+        n = (L.pkv_decode_shared_prefix_workspace_size(S, H, D, G, mc, partition_tokens) if G
+             else workspace_size(S, H, D, mc, partition_tokens))
+        workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
     L.pkv_decode_step(out, q, key, value, k_cache, v_cache, block_tables, context_lens, seq_idx,
-                      pos, slot_mapping, T, S, H, D, bs, NB, MB, max_context_len, scale,
-                      dtype_code(q.dtype), partition_tokens, workspace, workspace.numel(), stream)
+                      pos, slot_mapping, prefix_groups, G, T, S, H, D, bs, NB, MB,
+                      max_context_len, scale, dtype_code(q.dtype), partition_tokens, workspace,
+                      workspace.numel(), stream)
     return out
 
 
@@ -205,6 +210,9 @@ class DecodeStep:
         self.workspace = new_workspace(S, H, D, self.max_context_len, partition_tokens, dev)
         self.block_tables = None
         self.pairs = None
+        # shared-prefix groups [G, 3] int32 on the device for run(fused=True)
+        # (the workspace must then have the shared-prefix size)
+        self.prefix_groups = None
 
     def plan(self):
         """Host allocator: tables and copy-on-write pairs for this step."""
@@ -223,16 +231,19 @@ class DecodeStep:
     def run(self, stream=None, attention=True, write=True, fused=False):
         """The device part of the step: copy_blocks, slot mapping, cache
         write, decode.  fused=True runs the last three as pkv_decode_step
-        (two kernels instead of four, the same results)."""
+        (fewer kernels, the same results), with the shared-prefix decode
+        when self.prefix_groups is set."""
         if self.block_tables is None:
             self.plan()
         if fused and write and attention:
             if self.pairs.shape[0]:
                 copy_blocks(self.k_cache, self.v_cache, self.pairs, stream)
+            g = self.prefix_groups
             L.pkv_decode_step(self.out, self.q, self.new_k, self.new_v, self.k_cache, self.v_cache,
                               self.block_tables, self.context_lens, self.seq_idx, self.pos,
-                              self.slot_mapping, self.T, self.S, self.H, self.D, self.bs, self.NB,
-                              self.MB, self.max_context_len, self.scale, dtype_code(self.dtype),
+                              self.slot_mapping, g, 0 if g is None else int(g.shape[0]), self.T,
+                              self.S, self.H, self.D, self.bs, self.NB, self.MB,
+                              self.max_context_len, self.scale, dtype_code(self.dtype),
                               self.partition_tokens, self.workspace, self.workspace.numel(),
                               stream)
             return self.out

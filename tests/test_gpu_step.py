@@ -94,3 +94,34 @@ def test_fused_step_flags_bad_positions_like_the_slot_kernel():
 def test_fused_step_without_new_tokens_is_a_plain_decode():
     w = W.small_case(65, S=4, H=4, D=128, bs=16, ctx_lo=1, ctx_hi=300, n_new=0)
     compare_step(w, fused=True)
+
+
+@pytest.mark.parametrize("pt", [0, 64])
+def test_fused_step_with_prefix_groups(pt):
+    """With prefix groups the fused step equals copy_blocks + slot mapping +
+    cache write + shared-prefix decode bit for bit, and the oracle."""
+    from oracle import step as OS
+    from tests.gpu_harness import assert_attention_close, out_to_double
+    w = W.shared_prefix(cow=True, prompts=3, samples=4, prefix=128, tail_lo=1, tail_hi=40)
+    groups = np.array([[p * 4, 4, 128] for p in range(3)], dtype=np.int32)
+    st = device_step(w, pt)
+    st.plan()
+    k0, v0 = st.k_cache.clone(), st.v_cache.clone()
+    st.run(attention=False)
+    st.decode_shared_prefix(groups)
+    torch.cuda.synchronize()
+    want = [t.clone() for t in (st.slot_mapping, st.k_cache, st.v_cache, st.out)]
+    st.k_cache.copy_(k0)
+    st.v_cache.copy_(v0)
+    st.out.fill_(float("nan"))
+    st.slot_mapping.fill_(-7)
+    st.prefix_groups = torch.from_numpy(groups).cuda()
+    st.workspace = torch.empty(L.pkv_decode_shared_prefix_workspace_size(
+        w.S, w.H, w.D, len(groups), st.max_context_len, pt), dtype=torch.uint8, device="cuda")
+    st.run(fused=True)
+    torch.cuda.synchronize()
+    got = (st.slot_mapping, st.k_cache, st.v_cache, st.out)
+    for name, a, b in zip(("slots", "k_cache", "v_cache", "out"), want, got):
+        assert torch.equal(a.view(torch.int16) if a.dtype != torch.int64 else a,
+                           b.view(torch.int16) if b.dtype != torch.int64 else b), name
+    assert_attention_close(out_to_double(st.out), OS.run(w).out, f"fused shared prefix pt{pt}")
