@@ -102,9 +102,9 @@ int main(void) {
     for (int s = 0; s < S; ++s) pos[s] = ctx_before[s];
 
     /* device buffers */
-    void *dk, *dv, *dq, *dkey, *dval, *dout, *dout2, *dws;
+    void *dk, *dv, *dq, *dkey, *dval, *dout, *dout2, *dws, *dk2, *dv2, *dout3;
     int32_t *dbt, *dctx, *dseq, *dpos;
-    int64_t* dslot;
+    int64_t *dslot, *dslot2;
     const size_t ws = pkv_decode_workspace_size(S, H, D, MB * BS, 0);
     CHECK_CUDA(cudaMalloc(&dk, cache_elems * 2));
     CHECK_CUDA(cudaMalloc(&dv, cache_elems * 2));
@@ -119,6 +119,13 @@ int main(void) {
     CHECK_CUDA(cudaMalloc((void**)&dseq, sizeof seq_idx));
     CHECK_CUDA(cudaMalloc((void**)&dpos, sizeof pos));
     CHECK_CUDA(cudaMalloc((void**)&dslot, S * sizeof(int64_t)));
+    /* a second copy of the caches for the fused step */
+    CHECK_CUDA(cudaMalloc(&dk2, cache_elems * 2));
+    CHECK_CUDA(cudaMalloc(&dv2, cache_elems * 2));
+    CHECK_CUDA(cudaMalloc(&dout3, sizeof q));
+    CHECK_CUDA(cudaMalloc((void**)&dslot2, S * sizeof(int64_t)));
+    CHECK_CUDA(cudaMemcpy(dk2, kc, cache_elems * 2, cudaMemcpyHostToDevice));
+    CHECK_CUDA(cudaMemcpy(dv2, vc, cache_elems * 2, cudaMemcpyHostToDevice));
     CHECK_CUDA(cudaMemcpy(dk, kc, cache_elems * 2, cudaMemcpyHostToDevice));
     CHECK_CUDA(cudaMemcpy(dv, vc, cache_elems * 2, cudaMemcpyHostToDevice));
     CHECK_CUDA(cudaMemcpy(dq, q, sizeof q, cudaMemcpyHostToDevice));
@@ -137,6 +144,9 @@ int main(void) {
                                          PKV_F16, 0, dws, ws, NULL));
     CHECK_PKV(pkv_paged_attention_decode_noalloc(dout2, dq, dk, dv, dbt, dctx, S, H, D, BS, NB, MB, 0,
                                                  scale, PKV_F16, 0, NULL));
+    /* the same step in one call, on the second copy of the caches */
+    CHECK_PKV(pkv_decode_step(dout3, dq, dkey, dval, dk2, dv2, dbt, dctx, dseq, dpos, dslot2, NULL, 0,
+                              S, S, H, D, BS, NB, MB, 0, scale, PKV_F16, 0, dws, ws, NULL));
     CHECK_PKV(pkv_sync_check(NULL));
     int32_t flags = -1;
     CHECK_PKV(pkv_get_device_errors(&flags));
@@ -153,9 +163,19 @@ int main(void) {
     if (memcmp(kg, kc, cache_elems * 2)) { fprintf(stderr, "K cache differs\n"); return 1; }
     double ref[S * H * D];
     oracle_decode(ref, q, kc, vc, tables, ctx, S, H, D, BS, MB, scale, 0, NULL, NULL, 0, 1);
-    uint16_t got[S * H * D], got2[S * H * D];
+    uint16_t got[S * H * D], got2[S * H * D], got3[S * H * D];
     CHECK_CUDA(cudaMemcpy(got, dout, sizeof got, cudaMemcpyDeviceToHost));
     CHECK_CUDA(cudaMemcpy(got2, dout2, sizeof got2, cudaMemcpyDeviceToHost));
+    CHECK_CUDA(cudaMemcpy(got3, dout3, sizeof got3, cudaMemcpyDeviceToHost));
+    /* the fused step gives the separate calls' slots, caches and output bit for bit */
+    int64_t slot_fused[S];
+    CHECK_CUDA(cudaMemcpy(slot_fused, dslot2, sizeof slot_fused, cudaMemcpyDeviceToHost));
+    if (memcmp(slot_fused, slot_gpu, sizeof slot_fused)) { fprintf(stderr, "fused slots differ\n"); return 1; }
+    uint16_t* kg2 = malloc(cache_elems * 2);
+    CHECK_CUDA(cudaMemcpy(kg2, dk2, cache_elems * 2, cudaMemcpyDeviceToHost));
+    if (memcmp(kg2, kg, cache_elems * 2)) { fprintf(stderr, "fused K cache differs\n"); return 1; }
+    if (memcmp(got3, got, sizeof got)) { fprintf(stderr, "fused output differs\n"); return 1; }
+    free(kg2);
     double worst = 0.0;
     for (int i = 0; i < S * H * D; ++i) {
         double e1 = fabs(half_to_double(got[i]) - ref[i]), e2 = fabs(half_to_double(got2[i]) - ref[i]);
