@@ -160,7 +160,8 @@ class DecodeStep:
       n_new, new_k/new_v [T, H, D], seq_idx/pos [T]: the tokens appended;
       initial_free: the free list (last element handed out first).
     `plan()` runs the host allocator; `run()` launches copy_blocks, slot
-    mapping, reshape_and_cache and decode on `stream`.
+    mapping, reshape_and_cache and decode on `stream` (`run(fused=True)`:
+    copy_blocks and pkv_decode_step).
     """
 
     def __init__(self, *, dtype: str, S, H, D, bs, NB, MB, scale, ctx_before, n_new, tables_pre,
