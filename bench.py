@@ -301,10 +301,11 @@ def run_ours(args):
     from paged_kv_cache_162_gb300.engine import DecodeStep, dtype_code
 
     rank, world, local = dist_env()
-    if world > 1:
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if world > 1:
+        # one rank per GPU: bind the group to this rank's device
+        dist.init_process_group("nccl", device_id=dev)
 
     w = make_workload(args.workload, rank, args.block_size)
     st = DecodeStep(dtype=w.dtype, S=w.S, H=w.H, D=w.D, bs=w.bs, NB=w.NB, MB=w.MB, scale=w.scale,
@@ -367,7 +368,7 @@ def run_ours(args):
 
     def barrier():
         if world > 1:
-            dist.barrier()
+            dist.barrier(device_ids=[local])
 
     # ---- the timed region: K whole steps, events only at its two ends
     K = max(1, args.steps)
