@@ -53,6 +53,8 @@ def parse_args(argv=None):
                    help="llama7b_batch64 only: another block size (8, 16, 32, 64)")
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--prefix-kernel", choices=["mma", "tcgen05"], default="mma",
+                   help="with --shared-prefix: the prefix kernel (tcgen05: head_dim 128)")
     p.add_argument("--unfused", action="store_true",
                    help="time the step as four separate calls instead of pkv_decode_step")
     p.add_argument("--measure", choices=["step", "swap_blocks", "beam_search"], default="step",
@@ -292,6 +294,10 @@ def run_reference(args):
 
 # ------------------------------------------------------------- our path
 def run_ours(args):
+    if args.prefix_kernel == "tcgen05":
+        os.environ["PKV_PREFIX_KERNEL"] = "tcgen05"
+    else:
+        os.environ.pop("PKV_PREFIX_KERNEL", None)
     import numpy as np
     import torch
     import torch.distributed as dist
@@ -489,7 +495,8 @@ def run_ours(args):
                           f"vs 129 MB L2; no flush",
                     "parallelism": f"replicas{world}" if world > 1 else "single GPU",
                     "step_calls": ("copy_blocks (if any pairs) + pkv_decode_step"
-                                   + (" with prefix groups" if args.shared_prefix else "")
+                                   + (f" with prefix groups ({args.prefix_kernel} prefix kernel)"
+                                      if args.shared_prefix else "")
                                    if fused else
                                    "copy_blocks, compute_slot_mapping, reshape_and_cache, "
                                    "decode as separate calls"),

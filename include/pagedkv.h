@@ -65,6 +65,8 @@ typedef enum { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype;
 #define PKV_DEVERR_CONTEXT 0x4   /* context_len < 0 or > max context      */
 #define PKV_DEVERR_POSITION 0x8  /* slot mapping: position past the table */
 #define PKV_DEVERR_GROUP 0x10    /* shared-prefix group out of range      */
+#define PKV_DEVERR_TIMEOUT 0x20  /* a bounded wait inside a kernel ran out: the call's
+                                    results are not valid */
 
 /* Thread-local text of the last error ("" if none).  Never NULL. */
 const char* pkv_last_error_string(void);
@@ -169,7 +171,10 @@ pkv_status pkv_decode_step(
  *   workspace needs pkv_decode_shared_prefix_workspace_size(S, H, D, G,
  *   max_context_len, partition_tokens) bytes.
  * Only whole partitions inside a prefix are shared; a prefix shorter than a
- * partition is decoded as usual. */
+ * partition is decoded as usual.  The prefix runs on mma.sync by default;
+ * with PKV_PREFIX_KERNEL=tcgen05 in the environment (read on every call) and
+ * head_dim 128 it runs on tcgen05 with TMA loads instead (same results
+ * within the attention tolerance). */
 size_t pkv_decode_shared_prefix_workspace_size(int S, int H, int D, int G, int max_context_len,
                                                int partition_tokens);
 pkv_status pkv_paged_attention_decode_shared_prefix(

@@ -28,6 +28,7 @@ PKV_DEVERR_SLOT = 0x2
 PKV_DEVERR_CONTEXT = 0x4
 PKV_DEVERR_POSITION = 0x8
 PKV_DEVERR_GROUP = 0x10
+PKV_DEVERR_TIMEOUT = 0x20
 PKV_NOALLOC_SCRATCH_BYTES = 16 << 20
 PKV_SWAP_OUT = 0
 PKV_SWAP_IN = 1

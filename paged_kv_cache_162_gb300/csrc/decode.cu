@@ -42,9 +42,15 @@
 //  * Safety: a table entry outside [0, NB) or a context outside
 //    [0, max_context_len] is never dereferenced; the kernel masks it and
 //    sets a bit in the device error word.  No CTA ever waits on another.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "pagedkv.h"
 #include "pkv_device.cuh"
@@ -1105,6 +1111,8 @@ __global__ void __launch_bounds__(kThreads, 2) prefix_kernel(PrefixParams pp) {
     }
 }
 
+#include "prefix_tc.cuh"
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
@@ -1167,6 +1175,85 @@ int prefix_resident(PrefixFn fn, int D) {
     }
     if (used < 64) cache[used++] = {fn, dev, n};
     return n;
+}
+
+// ---- the tensor-core prefix kernel (head_dim 128) ----
+using PrefixTcFn = void (*)(PrefixParams, const CUtensorMap, const CUtensorMap);
+
+template <class E>
+PrefixTcFn pick_prefix_tc_bs(int bs) {
+    switch (bs) {
+        case 8: return prefix_tc_kernel<E, 8>;
+        case 16: return prefix_tc_kernel<E, 16>;
+        case 32: return prefix_tc_kernel<E, 32>;
+        default: return prefix_tc_kernel<E, 64>;
+    }
+}
+
+PrefixTcFn pick_prefix_tc(pkv_dtype dt, int bs) {
+    return dt == PKV_BF16 ? pick_prefix_tc_bs<pkv::BF16>(bs) : pick_prefix_tc_bs<pkv::F16>(bs);
+}
+
+// The cache as a 3-D tensor [NB*bs rows][H heads][128 dims] of 16-bit
+// elements; a box is min(bs, 16) rows (one block holds them) x 1 head x 64
+// dims (128 bytes), 128-byte swizzle.
+pkv_status encode_cache_map(CUtensorMap* map, const void* cache, int H, int NB, int bs,
+                            pkv_dtype dtype) {
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    static std::mutex mu;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (!encode) {
+            cudaDriverEntryPointQueryResult q;
+            void* f = nullptr;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                                 &q) != cudaSuccess ||
+                !f || q != cudaDriverEntryPointSuccess) {
+                cudaGetLastError();
+                return pkv::fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+            }
+            encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        }
+    }
+    const cuuint64_t gdim[3] = {(cuuint64_t)kTcD, (cuuint64_t)H, (cuuint64_t)NB * bs};
+    const cuuint64_t gstride[2] = {(cuuint64_t)kTcD * 2, (cuuint64_t)H * kTcD * 2};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)(bs < 16 ? bs : 16)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapDataType dt =
+        dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if (encode(map, dt, 3, const_cast<void*>(cache), gdim, gstride, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return pkv::fail(PKV_ERR_CUDA, "tensor map encoding failed");
+    return PKV_OK;
+}
+
+// The shared-prefix decode runs the mma.sync prefix kernel, which measured
+// faster on this HBM-bound contraction; PKV_PREFIX_KERNEL=tcgen05 in the
+// environment selects the tensor-core (tcgen05, TMA) kernel for head_dim
+// 128 instead.  Read on every call.
+bool prefix_tc_selected() {
+    const char* e = std::getenv("PKV_PREFIX_KERNEL");
+    return e && std::strcmp(e, "tcgen05") == 0;
+}
+
+// Allows the tensor-core prefix kernel its shared memory (once per device).
+bool prefix_tc_ready(PrefixTcFn fn) {
+    static std::mutex mu;
+    static struct { PrefixTcFn fn; int dev; } done[64];
+    static int used = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < used; ++i)
+        if (done[i].fn == fn && done[i].dev == dev) return true;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (used < 64) done[used++] = {fn, dev};
+    return true;
 }
 
 int resident_ctas(KernelFn fn) {
@@ -1330,7 +1417,29 @@ pkv_status launch_decode(const char* who, const CallShape& cs, void* out, const 
         snprintf(msg, sizeof msg, "%s plan launch", who);
         return pkv::cuda_fail(e, msg);
     }
-    if (G > 0) {
+    if (G > 0 && D == kTcD && prefix_tc_selected()) {
+        PrefixTcFn tfn = pick_prefix_tc(dtype, bs);
+        if (!prefix_tc_ready(tfn)) return pkv::fail(PKV_ERR_CUDA, "prefix_tc shared memory");
+        CUtensorMap tmk, tmv;
+        pkv_status ms = encode_cache_map(&tmk, k_cache, H, NB, bs, dtype);
+        if (ms == PKV_OK) ms = encode_cache_map(&tmv, v_cache, H, NB, bs, dtype);
+        if (ms != PKV_OK) return ms;
+        const int64_t pupper = (int64_t)(G > 0 ? G : 1) * cs.max_parts * p.HG;
+        const int64_t president = (int64_t)kTcCtasPerSm * pkv::sm_count();
+        PrefixParams pp;
+        pp.d = p;
+        pp.groups = groups;
+        pp.G = G;
+        cfg.gridDim = dim3((unsigned)(pupper < president ? pupper : president));
+        cfg.blockDim = dim3(kTcThreads);
+        cfg.dynamicSmemBytes = kTcSmemBytes;
+        e = cudaLaunchKernelEx(&cfg, tfn, pp, tmk, tmv);
+        if (e != cudaSuccess) {
+            snprintf(msg, sizeof msg, "%s prefix launch", who);
+            return pkv::cuda_fail(e, msg);
+        }
+        cfg.dynamicSmemBytes = 0;
+    } else if (G > 0) {
         PrefixFn pfn = pick_prefix(dtype, D, bs);
         const int per_sm = prefix_resident(pfn, D);
         if (per_sm < 1) return pkv::fail(PKV_ERR_CUDA, "prefix kernel cannot be resident");

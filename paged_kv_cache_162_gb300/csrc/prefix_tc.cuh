@@ -1,0 +1,621 @@
+// Shared-prefix decode on the 5th-generation tensor cores (head_dim 128).
+// Included by decode.cu inside its anonymous namespace: it uses that file's
+// Workspace, DecodeParams, PrefixParams and merge_partitions.
+//
+// Two CTAs of 6 warps per SM take the same work items as prefix_kernel --
+// (group, prefix partition, group of 4 heads) -- in a static order (the
+// items are all the same size), and for each head run
+//
+//   S^T = K Q^T    tcgen05.mma kind::f16, M = 128 tokens, N = 16 members,
+//                  K = 128 dims; A = a K tile (K-major), B = Q (K-major);
+//                  accumulator in TMEM, one 16-column slice per tile, two
+//                  buffers so the next chunk's scores overlap this softmax
+//   softmax        warps 0-3, one token per TMEM lane (tcgen05.ld); max and
+//                  sum per member across the warps; P rounded to 16 bits
+//                  into shared memory in the B layout of the next product
+//   O^T += V^T P^T tcgen05.mma, M = 128 dims, N = 16 members, K = 128
+//                  tokens; A = a V tile read MN-major, B = P (K-major)
+//
+// Warp 4 loads: K and V tiles of 128 tokens by TMA (cp.async.bulk.tensor,
+// boxes of min(bs, 16) rows x 128 bytes, 128-byte swizzle; the lanes look up
+// their blocks and issue their boxes together) into a 3-stage ring with a
+// full and an empty mbarrier per stage.  Warp 5 issues the MMAs (one
+// thread).  mbarriers hand each chunk and head between the roles.  Each
+// member's (max, sum, output) partial goes to the decode kernel's workspace
+// slots and the same tickets merge it.
+//
+// Every wait is bounded: on a timeout the roles stop, the kernel sets
+// PKV_DEVERR_TIMEOUT, waits (bounded) for its loads in flight, frees its
+// TMEM and returns.
+
+constexpr int kTcD = 128;                       // head_dim of this path
+constexpr int kTcTile = 128;                    // tokens per K or V tile
+constexpr int kTcCtasPerSm = 2;                 // CTAs resident per SM
+constexpr int kTcStages = 3;                    // tiles in flight per CTA
+constexpr int kTcChunkTiles = 2;                // tiles per softmax chunk
+constexpr int kTcHalf = kTcTile * 128;          // bytes of one 64-dim half of a tile (16 KB)
+constexpr int kTcTileBytes = 2 * kTcHalf;       // 32 KB
+constexpr int kTcQOff = kTcStages * kTcTileBytes;       // Q: 16 rows x 256 B (2 halves of 2 KB)
+constexpr int kTcPOff = kTcQOff + 4096;                 // P: chunk tiles x 4 KB
+constexpr int kTcBarOff = kTcPOff + kTcChunkTiles * 4096;
+constexpr int kTcSmemBytes = kTcBarOff + 1024 + 1024;   // barriers, TMEM slot, reductions; +1 KB alignment
+constexpr int kTcSCols = 16 * kTcChunkTiles;    // TMEM columns of one S buffer
+constexpr int kTcOCol = 2 * kTcSCols;           // O after the two S buffers
+constexpr int kTcTmemCols = kTcOCol + 16 <= 32 ? 32 : kTcOCol + 16 <= 64 ? 64
+                          : kTcOCol + 16 <= 128 ? 128 : kTcOCol + 16 <= 256 ? 256 : 512;
+constexpr long long kTcWaitLimit = 1ll << 20;   // try_wait rounds before giving up
+constexpr int kTcThreads = 192;                 // warps 0-3 softmax, 4 loads, 5 MMAs
+
+static_assert(kTcCtasPerSm * (kTcSmemBytes + 1024) <= 228 * 1024, "prefix_tc shared memory");
+static_assert(16 * kTcStages + 72 + 4 <= 256, "prefix_tc barriers overlap the reductions");
+static_assert(kTcCtasPerSm * kTcTmemCols <= 512, "prefix_tc TMEM");
+
+// ---- PTX helpers ----------------------------------------------------------
+__device__ __forceinline__ void tc_mbar_init(uint32_t bar, int count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void tc_mbar_expect(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool tc_mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// bounded wait for phase `parity`; false after kTcWaitLimit rounds or as
+// soon as another role has given up (*abort set)
+__device__ __forceinline__ bool tc_mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort) {
+    for (long long i = 0; i < kTcWaitLimit; ++i) {
+        if (tc_mbar_try(bar, parity)) return true;
+        if ((i & 255) == 255 && *abort) return false;
+    }
+    return false;
+}
+__device__ __forceinline__ void tc_tma_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+// UMMA shared-memory descriptor: 128-byte swizzle, sm_100 family version 1
+__device__ __forceinline__ uint64_t tc_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// instruction descriptor of kind::f16: fp32 accumulate, A/B f16 or bf16,
+// A K-major (0) or MN-major (1), B K-major, N = 16, M = 128
+template <class E>
+__device__ __forceinline__ uint32_t tc_idesc(uint32_t a_mn_major) {
+    constexpr uint32_t fmt = std::is_same<E, pkv::BF16>::value ? 1u : 0u;
+    return (1u << 4) | (fmt << 7) | (fmt << 10) | (a_mn_major << 15) | ((16u >> 3) << 17) |
+           ((128u >> 4) << 24);
+}
+__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t ad, uint64_t bd, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+        ::"r"(tmem_d), "l"(ad), "l"(bd), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// the mbarrier arrives once every tcgen05.mma issued so far has completed
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const float (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])),
+          "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])),
+          "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+          "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
+          "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
+          "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// generic-proxy writes to shared memory visible to the tensor cores
+__device__ __forceinline__ void tc_fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// byte offset of (row, element) in a 128-byte-swizzled K-major tile whose
+// rows hold 64 16-bit elements (8-row atoms of 1 KB)
+__device__ __forceinline__ uint32_t tc_sw128(int row, int el) {
+    return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((((el * 2) >> 4) ^ (row & 7)) << 4) +
+                      ((el * 2) & 15));
+}
+
+
+// ---- the kernel -----------------------------------------------------------
+// Items are the same size, so each CTA takes items b, b + grid, b + 2*grid,
+// ... and every role walks that sequence on its own.  Per item, per head,
+// per softmax chunk of up to 8 tiles:
+//   loader warp 4    K tiles of the chunk, then its V tiles, into the ring
+//   MMA warp 5       S^T slices (K tiles), commit s_ready; wait p_ready;
+//                    O^T += V^T P^T (V tiles); after the head: commit o_ready
+//   softmax warps    wait s_ready: max, P, sums, rescale O; arrive p_ready;
+//   0-3              after the head: wait o_ready, write the partials,
+//                    arrive o_free; before each head: Q, arrive q_ready
+struct TcItem {
+    int hg, part, first, n, nh;
+    const int32_t* bt_row;
+};
+
+__device__ __forceinline__ TcItem tc_item(const PrefixParams& pp, int it) {
+    const DecodeParams& a = pp.d;
+    TcItem r;
+    r.hg = it % a.HG;
+    const int packed = a.ws.pitems[it / a.HG];
+    const int gi = packed >> 16;
+    r.part = packed & 0xffff;
+    r.first = pp.groups[3 * gi];
+    r.n = pp.groups[3 * gi + 1];
+    r.nh = min(kWarps, a.H - r.hg * kWarps);
+    r.bt_row = a.block_tables + (int64_t)r.first * a.MB;
+    return r;
+}
+
+template <class E, int BS>
+__global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
+prefix_tc_kernel(PrefixParams pp, const __grid_constant__ CUtensorMap tmk,
+                 const __grid_constant__ CUtensorMap tmv) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    extern __shared__ unsigned char tc_raw[];
+    const uint32_t raw = (uint32_t)__cvta_generic_to_shared(tc_raw);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    unsigned char* smem = tc_raw + pad;
+    const uint32_t sb = raw + pad;  // 1024-byte aligned: the swizzle atoms line up
+    const DecodeParams& a = pp.d;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // barriers: full and empty per stage, then the hand-offs between roles
+    const uint32_t bar_full = sb + kTcBarOff;
+    const uint32_t bar_empty = bar_full + 8 * kTcStages;
+    const uint32_t bar_q = bar_empty + 8 * kTcStages;  // Q written (128 arrivals)
+    const uint32_t bar_s0 = bar_q + 8;                 // S buffer 0 ready (commit)
+    const uint32_t bar_s1 = bar_s0 + 8;                // S buffer 1 ready (commit)
+    const uint32_t bar_p = bar_s1 + 8;                 // P written, O rescaled (128)
+    const uint32_t bar_pv = bar_p + 8;                 // a chunk's P.V done (commit)
+    const uint32_t bar_o = bar_pv + 8;                 // O complete (commit)
+    const uint32_t bar_of = bar_o + 8;                 // O read out (128)
+    const uint32_t bar_end = bar_of + 8;               // final commit
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kTcBarOff + 16 * kTcStages + 72);
+    float* red = reinterpret_cast<float*>(smem + kTcBarOff + 256);  // [4 warps][16]
+    float* mrun = red + 64;
+    float* lrun = mrun + 16;
+    float* corr = lrun + 16;
+    float* mnew = corr + 16;
+    // [0] abort, [1] last-partition bits, [2] tiles consumed, [4] tiles issued
+    volatile int* sh = reinterpret_cast<volatile int*>(mnew + 16);
+
+    const int PT = *a.ws.pt;
+    const int nt = (PT + kTcTile - 1) / kTcTile;
+    const int total = *a.ws.n_pitems * a.HG;
+    constexpr int R = BS < 16 ? BS : 16;  // rows per TMA box (one block holds them)
+
+    // zero the ring and P once: rows a tile does not load stay finite
+    for (int i = tid; i < kTcBarOff / 16; i += kTcThreads)
+        reinterpret_cast<uint4*>(smem)[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (tid == 0) {
+        for (int s = 0; s < kTcStages; ++s) {
+            tc_mbar_init(bar_full + 8 * s, 1);
+            tc_mbar_init(bar_empty + 8 * s, 1);
+        }
+        tc_mbar_init(bar_q, 128);
+        tc_mbar_init(bar_s0, 1);
+        tc_mbar_init(bar_s1, 1);
+        tc_mbar_init(bar_p, 128);
+        tc_mbar_init(bar_pv, 1);
+        tc_mbar_init(bar_o, 1);
+        tc_mbar_init(bar_of, 128);
+        tc_mbar_init(bar_end, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        sh[0] = 0;
+        sh[2] = 0;
+        sh[4] = 0;
+        sh[5] = 0;
+    }
+    tc_fence_async_smem();
+    __syncthreads();
+    if (warp == 5) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(sb + kTcBarOff + 16 * kTcStages + 72), "r"(kTcTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    auto fail = [&]() { sh[0] = 1; };
+
+    if (warp == 4) {
+        // ---------------- loader: lanes look up blocks and issue boxes together
+        constexpr int kRowBoxes = kTcTile / R;  // boxes per 64-dim half
+        long long g = 0;
+        bool stop = false;  // the same in every lane (decided by lane 0)
+        const int nch = (nt + kTcChunkTiles - 1) / kTcChunkTiles;
+        // the tiles of one chunk (kind 0: K, 1: V) of head h, each into the
+        // next stage of the ring
+        auto emit = [&](const TcItem& item, int h, int kind, int ch) {
+            const CUtensorMap* map = kind == 0 ? &tmk : &tmv;
+            const int t1 = min((ch + 1) * kTcChunkTiles, nt);
+            for (int t = ch * kTcChunkTiles; t < t1 && !stop; ++t) {
+                const int stage = (int)(g % kTcStages);
+                int ok = 1;
+                if (lane == 0) {
+                    if (g >= kTcStages)
+                        ok = tc_mbar_wait(bar_empty + 8 * stage,
+                                          (uint32_t)(((g / kTcStages) - 1) & 1), sh) ? 1 : 0;
+                    if (sh[0]) ok = 0;
+                }
+                ok = __shfl_sync(kFull, ok, 0);
+                if (!ok) {
+                    if (lane == 0) fail();
+                    stop = true;
+                    break;
+                }
+                // lane l: box (half l / kRowBoxes, rows R*(l % kRowBoxes) ..)
+                const int half = lane / kRowBoxes, rb = lane % kRowBoxes;
+                int row = -1;
+                if (half < 2 && rb * R < PT - t * kTcTile) {
+                    const int tok = item.part * PT + t * kTcTile + rb * R;
+                    const int p = __ldg(item.bt_row + tok / BS);
+                    if ((unsigned)p < (unsigned)a.NB) row = p * BS + tok % BS;
+                    else pkv::report(a.err, PKV_DEVERR_BLOCK_ID);
+                }
+                const unsigned boxes = __popc(__ballot_sync(kFull, row >= 0));
+                const uint32_t full = bar_full + 8 * stage;
+                if (lane == 0) tc_mbar_expect(full, boxes * (uint32_t)(R * 128));
+                __syncwarp();
+                if (row >= 0)
+                    tc_tma_3d(sb + (uint32_t)stage * kTcTileBytes + half * kTcHalf + rb * R * 128,
+                              map, half * 64, h, row, full);
+                ++g;
+            }
+        };
+        // per head: K of chunk 0, then for each chunk c: K of chunk c+1, V of
+        // chunk c -- the order in which the MMA warp takes them
+        for (int it = blockIdx.x; it < total && !stop; it += gridDim.x) {
+            const TcItem item = tc_item(pp, it);
+            for (int j = 0; j < item.nh && !stop; ++j) {
+                const int h = item.hg * kWarps + j;
+                emit(item, h, 0, 0);
+                for (int c = 0; c < nch && !stop; ++c) {
+                    if (c + 1 < nch) emit(item, h, 0, c + 1);
+                    emit(item, h, 1, c);
+                }
+            }
+        }
+        if (lane == 0) sh[4] = (int)g;  // tiles issued
+    }
+    else if (warp == 5) {
+        // ---------------- MMAs: one thread issues, the tensor cores run async
+        if (lane == 0) {
+            const uint32_t idesc_k = tc_idesc<E>(0u), idesc_v = tc_idesc<E>(1u);
+            const int nch = (nt + kTcChunkTiles - 1) / kTcChunkTiles;
+            long long g = 0;
+            uint32_t heads = 0, chunks = 0;  // chunks: global index of the head's chunk 0
+            bool ok = true;
+            // S^T of chunk k (global index) into S buffer k & 1; commit s[k & 1]
+            auto s_chunk = [&](int c, uint32_t k) -> bool {
+                const int nc = min(kTcChunkTiles, nt - c * kTcChunkTiles);
+                const uint32_t cols = tmem + (k & 1u) * kTcSCols;
+                for (int i = 0; i < nc; ++i, ++g) {
+                    const int stage = (int)(g % kTcStages);
+                    if (!tc_mbar_wait(bar_full + 8 * stage, (uint32_t)((g / kTcStages) & 1), sh)) return false;
+                    tc_fence_after();
+                    const uint32_t tile = sb + (uint32_t)stage * kTcTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kTcD / 16; ++kk) {
+                        const uint64_t ad = tc_desc(tile + (kk >> 2) * kTcHalf + (kk & 3) * 32, 16, 1024);
+                        const uint64_t bd = tc_desc(sb + kTcQOff + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024);
+                        tc_mma(cols + 16 * i, ad, bd, idesc_k, kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(bar_empty + 8 * stage);
+                }
+                tc_commit((k & 1u) ? bar_s1 : bar_s0);
+                return true;
+            };
+            // O^T += V^T P^T over chunk c; commit pv
+            auto pv_chunk = [&](int c, uint32_t k) -> bool {
+                const int nc = min(kTcChunkTiles, nt - c * kTcChunkTiles);
+                const uint32_t pbuf = sb + kTcPOff;
+                for (int i = 0; i < nc; ++i, ++g) {
+                    const int stage = (int)(g % kTcStages);
+                    if (!tc_mbar_wait(bar_full + 8 * stage, (uint32_t)((g / kTcStages) & 1), sh)) return false;
+                    tc_fence_after();
+                    const uint32_t tile = sb + (uint32_t)stage * kTcTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kTcTile / 16; ++kk) {
+                        const uint64_t ad = tc_desc(tile + kk * 2048, kTcHalf, 1024);
+                        const uint64_t bd = tc_desc(pbuf + i * 4096 + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024);
+                        tc_mma(tmem + kTcOCol, ad, bd, idesc_v, (c > 0 || i > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(bar_empty + 8 * stage);
+                }
+                tc_commit(bar_pv);
+                return true;
+            };
+            for (int it = blockIdx.x; ok && it < total; it += gridDim.x) {
+                const TcItem item = tc_item(pp, it);
+                for (int j = 0; ok && j < item.nh; ++j, ++heads) {
+                    ok = tc_mbar_wait(bar_q, heads & 1u, sh);  // this head's Q
+                    if (ok) tc_fence_after();
+                    ok = ok && s_chunk(0, chunks);
+                    for (int c = 0; ok && c < nch; ++c) {
+                        // the next chunk's scores while the softmax works on this one
+                        if (c + 1 < nch) ok = s_chunk(c + 1, chunks + c + 1);
+                        ok = ok && tc_mbar_wait(bar_p, (chunks + c) & 1u, sh);  // P written, O rescaled
+                        if (ok) tc_fence_after();
+                        ok = ok && pv_chunk(c, chunks + c);
+                    }
+                    chunks += nch;
+                    if (!ok) break;
+                    tc_commit(bar_o);
+                    ok = tc_mbar_wait(bar_of, heads & 1u, sh);  // O read out
+                }
+            }
+            if (!ok) fail();
+            tc_commit(bar_end);  // every MMA issued so far
+            tc_mbar_wait(bar_end, 0u, sh + 5);
+            sh[2] = (int)g;  // tiles consumed
+        }
+    }
+    else {
+        // ---------------- softmax and epilogue: warps 0-3, one TMEM lane each
+        const int row = 32 * warp + lane;  // a token of a tile, then a dim of O
+        const uint32_t tlane = tmem + ((uint32_t)(32 * warp) << 16);
+        auto csync = [] { asm volatile("bar.sync 1, 128;" ::: "memory"); };  // these 4 warps only
+        // barrier over these 4 warps that also ANDs `ok`: all continue or all stop
+        auto csync_and = [](bool v) -> bool {
+            uint32_t r;
+            asm volatile(
+                "{.reg .pred p, q;\n\t"
+                "setp.ne.u32 p, %1, 0;\n\t"
+                "bar.red.and.pred q, 1, 128, p;\n\t"
+                "selp.u32 %0, 1, 0, q;}"
+                : "=r"(r)
+                : "r"(v ? 1u : 0u)
+                : "memory");
+            return r != 0;
+        };
+        uint32_t heads = 0, chunks = 0;
+        bool ok = true;
+        for (int it = blockIdx.x; ok && it < total; it += gridDim.x) {
+            const TcItem item = tc_item(pp, it);
+            for (int j = 0; ok && j < item.nh; ++j, ++heads) {
+                const int h = item.hg * kWarps + j;
+                // the members' queries (rows >= n zero) as the B operand
+                {
+                    const int m = row >> 3, d0 = (row & 7) * 16;
+                    uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+                    if (m < item.n) {
+                        const uint4* src = reinterpret_cast<const uint4*>(
+                            static_cast<const uint16_t*>(a.q) +
+                            ((int64_t)(item.first + m) * a.H + h) * kTcD + d0);
+                        v0 = __ldg(src);
+                        v1 = __ldg(src + 1);
+                    }
+                    const int c = (d0 & 63) >> 3;
+                    unsigned char* qb = smem + kTcQOff + (d0 >> 6) * 2048 + (m >> 3) * 1024 + (m & 7) * 128;
+                    *reinterpret_cast<uint4*>(qb + ((c ^ (m & 7)) << 4)) = v0;
+                    *reinterpret_cast<uint4*>(qb + (((c + 1) ^ (m & 7)) << 4)) = v1;
+                }
+                if (row < 16) {
+                    mrun[row] = -INFINITY;
+                    lrun[row] = 0.f;
+                }
+                tc_fence_async_smem();
+                tc_mbar_arrive(bar_q);
+                for (int c0 = 0; ok && c0 < nt; c0 += kTcChunkTiles, ++chunks) {
+                    const int nc = min(kTcChunkTiles, nt - c0);
+                    const uint32_t kb = chunks & 1u;  // this chunk's S buffer
+                    ok = csync_and(tc_mbar_wait(kb ? bar_s1 : bar_s0, (chunks >> 1) & 1u, sh));
+                    // the previous chunk's P.V: O is complete up to it, and
+                    // P's last reader is done
+                    if (ok && c0 > 0) ok = csync_and(tc_mbar_wait(bar_pv, (chunks - 1) & 1u, sh));
+                    if (!ok) break;
+                    tc_fence_after();
+                    // pass 1: the chunk's max per member; this thread's valid
+                    // tokens (inside the partition, block id in range)
+                    uint32_t vmask = 0;
+                    float mx[16];
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) mx[m] = -INFINITY;
+                    for (int i = 0; i < nc; ++i) {
+                        const int rel = (c0 + i) * kTcTile + row;
+                        bool valid = rel < PT;
+                        if (valid)
+                            valid = (unsigned)__ldg(item.bt_row + (item.part * PT + rel) / BS) <
+                                    (unsigned)a.NB;
+                        vmask |= valid ? (1u << i) : 0u;
+                        float s[16];
+                        tc_ld16(tlane + kb * kTcSCols + 16 * i, s);
+                        if (valid) {
+#pragma unroll
+                            for (int m = 0; m < 16; ++m) mx[m] = fmaxf(mx[m], s[m] * a.qscale);
+                        }
+                    }
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) {
+#pragma unroll
+                        for (int o = 16; o >= 1; o >>= 1) mx[m] = fmaxf(mx[m], __shfl_xor_sync(kFull, mx[m], o));
+                    }
+                    if (lane == 0) {
+#pragma unroll
+                        for (int m = 0; m < 16; ++m) red[warp * 16 + m] = mx[m];
+                    }
+                    csync();
+                    if (row < 16) {
+                        const float cm = fmaxf(fmaxf(red[row], red[16 + row]), fmaxf(red[32 + row], red[48 + row]));
+                        const float mo = mrun[row];
+                        float mn = fmaxf(mo, cm);
+                        if (mn == -INFINITY) mn = 0.f;  // nothing valid yet: any base works
+                        corr[row] = exp2f(mo - mn);
+                        mnew[row] = mn;
+                    }
+                    csync();
+                    // pass 2: P (16-bit) into shared memory, sums per member
+                    float mu[16], ls[16];
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) {
+                        mu[m] = mnew[m];
+                        ls[m] = 0.f;
+                    }
+                    for (int i = 0; i < nc; ++i) {
+                        float s[16];
+                        tc_ld16(tlane + kb * kTcSCols + 16 * i, s);
+                        const bool valid = (vmask >> i) & 1u;
+                        unsigned char* pb = smem + kTcPOff + i * 4096 + (row >> 6) * 2048;
+#pragma unroll
+                        for (int m = 0; m < 16; ++m) {
+                            const float p = valid ? exp2f(s[m] * a.qscale - mu[m]) : 0.f;
+                            ls[m] += p;
+                            *reinterpret_cast<uint16_t*>(pb + tc_sw128(m, row & 63)) =
+                                (uint16_t)(E::from_float2(p, 0.f) & 0xffffu);
+                        }
+                    }
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) {
+#pragma unroll
+                        for (int o = 16; o >= 1; o >>= 1) ls[m] += __shfl_xor_sync(kFull, ls[m], o);
+                    }
+                    if (lane == 0) {
+#pragma unroll
+                        for (int m = 0; m < 16; ++m) red[warp * 16 + m] = ls[m];
+                    }
+                    csync();
+                    if (row < 16) {
+                        lrun[row] = lrun[row] * corr[row] +
+                                    ((red[row] + red[16 + row]) + (red[32 + row] + red[48 + row]));
+                        mrun[row] = mnew[row];
+                    }
+                    // a later chunk rescales what O holds so far
+                    if (c0 > 0) {
+                        float o[16];
+                        tc_ld16(tlane + kTcOCol, o);
+#pragma unroll
+                        for (int m = 0; m < 16; ++m) o[m] *= corr[m];
+                        tc_st16(tlane + kTcOCol, o);
+                    }
+                    csync();  // running sums settled before the next chunk reads red
+                    tc_fence_async_smem();
+                    tc_fence_before();
+                    tc_mbar_arrive(bar_p);
+                }
+                if (!ok) break;
+                ok = csync_and(tc_mbar_wait(bar_o, heads & 1u, sh));
+                if (!ok) break;
+                tc_fence_after();
+                {
+                    float o[16];
+                    tc_ld16(tlane + kTcOCol, o);
+                    const int d = row;
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) {
+                        if (m < item.n) {
+                            const int s = item.first + m;
+                            const int np = a.ws.nparts[s];
+                            if (np == 1) {
+                                const float l = lrun[m];
+                                const float inv = l > 0.f ? 1.f / l : 0.f;
+                                static_cast<uint16_t*>(a.out)[((int64_t)s * a.H + h) * kTcD + d] =
+                                    (uint16_t)(E::from_float2(o[m] * inv, 0.f) & 0xffffu);
+                            } else {
+                                const int64_t idx = ((int64_t)s * a.H + h) * a.max_parts + item.part;
+                                a.ws.acc[idx * kTcD + d] = o[m];
+                                if (d == 0) {
+                                    a.ws.m[idx] = mrun[m];
+                                    a.ws.l[idx] = lrun[m];
+                                }
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                tc_mbar_arrive(bar_of);
+            }
+            if (!ok) break;
+            // tickets of the members that have more than one partition
+            __threadfence();
+            csync();
+            if (row < 16) {
+                unsigned bit = 0;
+                if (row < item.n) {
+                    const int s = item.first + row;
+                    const int np = a.ws.nparts[s];
+                    if (np > 1) {
+                        const unsigned done = atomicAdd(&a.ws.tickets[s * a.HG + item.hg], 1u);
+                        bit = (done == (unsigned)(np - 1)) ? (1u << row) : 0u;
+                    }
+                }
+#pragma unroll
+                for (int o = 8; o >= 1; o >>= 1) bit |= __shfl_xor_sync(0xffffu, bit, o);
+                if (row == 0) sh[1] = (int)bit;
+            }
+            csync();
+            unsigned last = (unsigned)sh[1];
+            if (last) {
+                __threadfence();
+                const int h = item.hg * kWarps + warp;
+                while (last) {
+                    const int m = __ffs(last) - 1;
+                    last &= last - 1;
+                    if (h < a.H) merge_partitions<E, kTcD>(a, item.first + m, h, a.ws.nparts[item.first + m], lane);
+                }
+            }
+            csync();  // sh[1] read by all before the next item writes it
+        }
+        if (!ok) fail();
+    }
+
+    // every role is done: loads still in flight (only after a timeout) land,
+    // then TMEM is freed
+    __syncthreads();
+    if (warp == 4 && lane == 0) {
+        for (long long k = sh[2]; k < sh[4]; ++k)
+            tc_mbar_wait(bar_full + 8 * (int)(k % kTcStages), (uint32_t)((k / kTcStages) & 1), sh + 5);
+        if (sh[0]) pkv::report(a.err, PKV_DEVERR_TIMEOUT);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 5) {
+        __syncwarp();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcTmemCols)
+                     : "memory");
+    }
+}

@@ -12,6 +12,17 @@ from tests.gpu_harness import assert_attention_close, compare_step, device_step,
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(params=["mma", "tcgen05"], autouse=True)
+def prefix_kernel(request, monkeypatch):
+    """Every test runs with the default prefix kernel and with the
+    tensor-core one (which serves head_dim 128)."""
+    if request.param == "tcgen05":
+        monkeypatch.setenv("PKV_PREFIX_KERNEL", "tcgen05")
+    else:
+        monkeypatch.delenv("PKV_PREFIX_KERNEL", raising=False)
+    return request.param
+
+
 def _groups(w, samples, prefix, every=1):
     prompts = w.S // samples
     return np.array([[p * samples, samples, prefix] for p in range(0, prompts, every)],
