@@ -32,13 +32,19 @@
 //    workspace; the CTA that finishes a (sequence, head group) last -- known
 //    from an atomic ticket, no waiting -- merges them.  A single-partition
 //    context writes its output directly.
-//  * Scheduling: a one-CTA plan kernel chooses the partition size, lists the
-//    (sequence, partition) items -- full partitions in sequence order, with
-//    the partial (last) partitions before or after them, see plan_kernel --
-//    and resets the work counter and tickets.  The decode kernel is
+//  * Scheduling: one CTA plans (plan_cta): it chooses the partition size,
+//    lists the (sequence, partition) items -- full partitions in sequence
+//    order, with the partial (last) partitions before or after them -- and
+//    resets the work counter and tickets.  The plan runs as plan_kernel, or
+//    as CTA 0 of step_prologue_kernel when a whole decode step (slot
+//    mapping, cache write, attention) is one call.  The decode kernel is
 //    persistent (as many CTAs as fit on the SMs) and takes items from the
 //    counter.  It is launched with programmatic dependent launch so its
-//    CTAs are resident when the plan kernel ends.
+//    CTAs are resident when the plan ends.
+//  * Shared prefixes: when sequences share the blocks of a prefix, a
+//    prefix kernel (mma.sync, or tcgen05 + TMA in prefix_tc.cuh) reads each
+//    shared block once for all members of the group; the decode kernel then
+//    covers only the members' own tokens, and the tickets merge both.
 //  * Safety: a table entry outside [0, NB) or a context outside
 //    [0, max_context_len] is never dereferenced; the kernel masks it and
 //    sets a bit in the device error word.  No CTA ever waits on another.

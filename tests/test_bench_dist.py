@@ -57,3 +57,27 @@ def test_weak_value_and_single_rank_identity():
     assert bench.reduce_max([1.0, 2.0], 1) == [1.0, 2.0]
     # two ranks each moving 1 GB in a 0.5 s (slowest) step: 4 GB/s job-wide
     assert np.isclose(bench.weak_value(1e9, 2, 500.0), 4.0)
+
+
+def test_source_digest_ignores_comments_only():
+    """The recorded ncu traffic stays valid across comment edits and is
+    dropped as soon as the code itself changes."""
+    src = ('// header\nint f(int x) { /* why */ return x + 1; }\n'
+           'const char* s = "a // not a comment /* nor this */";\n'
+           "char c = '\\'';  // trailing\n")
+    recommented = ('int f(int x) {\n    return x + 1;  // reason\n}\n'
+                   'const char* s = "a // not a comment /* nor this */";\n'
+                   "char c = '\\'';\n")
+    changed = src.replace("x + 1", "x + 2")
+    assert bench.strip_comments(src) == bench.strip_comments(recommented)
+    assert bench.strip_comments(src) != bench.strip_comments(changed)
+    assert "/* nor this */" in bench.strip_comments(src)
+    assert "why" not in bench.strip_comments(src)
+
+
+def test_profiled_traffic_matches_current_sources():
+    """The committed decode profile was taken on the decode code as it is;
+    if not, the bench reports roofline.traffic as null, and this says so."""
+    import pytest
+    if bench.profiled_traffic("llama7b_batch64") is None:
+        pytest.skip("decode code changed since the committed ncu capture: traffic reads null")
