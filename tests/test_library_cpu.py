@@ -37,6 +37,36 @@ def test_library_exports_every_declared_symbol():
         assert n in L.SIGNATURES, f"binding lacks {n}"
 
 
+def header_constants():
+    """Every PKV_* constant the header gives a value: #defines and enumerators."""
+    text = open(os.path.join(ROOT, "include", "pagedkv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    consts = {}
+    for name, val in re.findall(r"#define\s+(PKV_\w+)\s+(0x[0-9a-fA-F]+|[0-9]+)\b", text):
+        consts[name] = int(val, 0)
+    for name, val, shift in re.findall(r"#define\s+(PKV_\w+)\s+\(([0-9]+)u\s*<<\s*(\d+)\)", text):
+        consts[name] = int(val) << int(shift)
+    for name, val in re.findall(r"\b(PKV_\w+)\s*=\s*([0-9]+)", text):
+        consts[name] = int(val)
+    return consts
+
+
+def test_binding_constants_equal_the_header():
+    """The Python names carry the header's values, device error bits
+    included, so a bit read back from the device decodes the same way."""
+    consts = header_constants()
+    for name in ["PKV_OK", "PKV_ERR_INVALID_ARG", "PKV_ERR_UNSUPPORTED", "PKV_ERR_OOM",
+                 "PKV_ERR_WORKSPACE", "PKV_ERR_CUDA", "PKV_F16", "PKV_BF16",
+                 "PKV_DEVERR_BLOCK_ID", "PKV_DEVERR_SLOT", "PKV_DEVERR_CONTEXT",
+                 "PKV_DEVERR_POSITION", "PKV_DEVERR_GROUP", "PKV_DEVERR_TIMEOUT",
+                 "PKV_NOALLOC_SCRATCH_BYTES", "PKV_SWAP_OUT", "PKV_SWAP_IN"]:
+        assert name in consts, f"header lacks {name}"
+        assert getattr(L, name) == consts[name], name
+    bits = [v for k, v in consts.items() if k.startswith("PKV_DEVERR_")]
+    assert len(bits) == 6
+    assert all(b and b & (b - 1) == 0 for b in bits) and len(set(bits)) == len(bits)
+
+
 def test_version_and_workspace_size():
     assert "sm_103a" in P.pkv_version()
     ws = P.pkv_decode_workspace_size(64, 32, 128, 2048, 256)
