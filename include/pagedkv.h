@@ -127,8 +127,8 @@ pkv_status pkv_paged_attention_decode(
  * that of pkv_compute_slot_mapping, pkv_reshape_and_cache and
  * pkv_paged_attention_decode called in that order with the same arguments
  * (same slots, same cache contents, bit-identical output); it runs in two
- * kernels instead of four (three with prefix groups), the slot mapping, cache write and the decode's
- * work plan in one.  This fusion is this library's; the pages describe the
+ * kernels instead of four (three with prefix groups), the slot mapping,
+ * cache write and the decode's work plan in one.  This fusion is this library's; the pages describe the
  * three operations, not a combined call.
  *
  *   key, value    [T][H][D] dtype: K and V of the new tokens, 16-byte aligned
@@ -286,6 +286,18 @@ pkv_status pkv_sync_check(void* stream);
 /* Reads and clears the device error word (PKV_DEVERR_* bits) of the
  * current device.  Synchronises with the device. */
 pkv_status pkv_get_device_errors(int32_t* flags);
+
+/* Self-test of the give-up path of the library's in-kernel waits.  The
+ * tensor-core shared-prefix kernel (PKV_PREFIX_KERNEL=tcgen05) hands work
+ * between its warps through shared-memory barriers, and each wait there
+ * gives up after at most 2^20 polls (about 0.1 s on GB300): the CTA then
+ * sets PKV_DEVERR_TIMEOUT, frees its tensor memory and returns, and the
+ * context stays usable.  This call launches one warp on `stream` that takes
+ * tensor memory, waits `polls` polls on a barrier that nothing completes,
+ * sets PKV_DEVERR_TIMEOUT, frees the tensor memory and returns.
+ * Asynchronous; read the bit with pkv_get_device_errors.  `polls` outside
+ * [1, 2^20]: PKV_ERR_INVALID_ARG, nothing launched. */
+pkv_status pkv_selftest_bounded_wait(int64_t polls, void* stream);
 
 /* ------------------------------------------------------------------ *
  * Host block allocator: one global pool of physical blocks with a free

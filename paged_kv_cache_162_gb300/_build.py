@@ -21,7 +21,6 @@ LIB = os.path.join(PKG, "libpagedkv.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CU_SOURCES = ["runtime.cu", "cache_ops.cu", "decode.cu"]
 CXX_SOURCES = ["allocator.cpp"]
-HEADERS = ["pkv_device.cuh", "pkv_internal.h"]
 
 
 def cuda_home() -> str:
@@ -39,7 +38,10 @@ def _nvcc() -> str:
 
 
 def _inputs():
-    srcs = [os.path.join(CSRC, s) for s in CU_SOURCES + CXX_SOURCES + HEADERS]
+    """Every file the library is built from: all of csrc (sources and the
+    headers they include), the public header and this script."""
+    srcs = [os.path.join(CSRC, f) for f in sorted(os.listdir(CSRC))
+            if f.endswith((".cu", ".cuh", ".h", ".cpp"))]
     return srcs + [os.path.join(INCLUDE, "pagedkv.h"), os.path.abspath(__file__)]
 
 

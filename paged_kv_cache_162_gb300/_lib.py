@@ -73,6 +73,7 @@ SIGNATURES = {
     "pkv_swap_blocks": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "pkv_sync_check": (_I, [_P]),
     "pkv_get_device_errors": (_I, [_P]),
+    "pkv_selftest_bounded_wait": (_I, [ctypes.c_int64, _P]),
     "pkv_alloc_create": (_I, [_I32, _P]),
     "pkv_alloc_create_with_order": (_I, [_I32, _P, _I32, _P]),
     "pkv_alloc_destroy": (None, [_P]),
@@ -231,3 +232,8 @@ def pkv_get_device_errors() -> int:
     v = ctypes.c_int32(0)
     check(lib().pkv_get_device_errors(ctypes.addressof(v)), "get_device_errors")
     return int(v.value)
+
+
+def pkv_selftest_bounded_wait(polls: int, stream=None) -> None:
+    check(lib().pkv_selftest_bounded_wait(int(polls), stream_handle(stream)),
+          "selftest_bounded_wait")

@@ -28,6 +28,8 @@
 // PKV_DEVERR_TIMEOUT, waits (bounded) for its loads in flight, frees its
 // TMEM and returns.
 
+#include "tc_wait.cuh"
+
 constexpr int kTcD = 128;                       // head_dim of this path
 constexpr int kTcTile = 128;                    // tokens per K or V tile
 constexpr int kTcCtasPerSm = 2;                 // CTAs resident per SM
@@ -43,43 +45,19 @@ constexpr int kTcSCols = 16 * kTcChunkTiles;    // TMEM columns of one S buffer
 constexpr int kTcOCol = 2 * kTcSCols;           // O after the two S buffers
 constexpr int kTcTmemCols = kTcOCol + 16 <= 32 ? 32 : kTcOCol + 16 <= 64 ? 64
                           : kTcOCol + 16 <= 128 ? 128 : kTcOCol + 16 <= 256 ? 256 : 512;
-constexpr long long kTcWaitLimit = 1ll << 20;   // try_wait rounds before giving up
 constexpr int kTcThreads = 192;                 // warps 0-3 softmax, 4 loads, 5 MMAs
 
 static_assert(kTcCtasPerSm * (kTcSmemBytes + 1024) <= 228 * 1024, "prefix_tc shared memory");
 static_assert(16 * kTcStages + 72 + 4 <= 256, "prefix_tc barriers overlap the reductions");
 static_assert(kTcCtasPerSm * kTcTmemCols <= 512, "prefix_tc TMEM");
 
-// ---- PTX helpers ----------------------------------------------------------
-__device__ __forceinline__ void tc_mbar_init(uint32_t bar, int count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
+// ---- PTX helpers (the mbarrier waits and TMEM fences are in tc_wait.cuh) ---
 __device__ __forceinline__ void tc_mbar_expect(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
 }
 __device__ __forceinline__ void tc_mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool tc_mbar_try(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// bounded wait for phase `parity`; false after kTcWaitLimit rounds or as
-// soon as another role has given up (*abort set)
-__device__ __forceinline__ bool tc_mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort) {
-    for (long long i = 0; i < kTcWaitLimit; ++i) {
-        if (tc_mbar_try(bar, parity)) return true;
-        if ((i & 255) == 255 && *abort) return false;
-    }
-    return false;
 }
 __device__ __forceinline__ void tc_tma_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
                                           uint32_t bar) {
@@ -139,12 +117,6 @@ __device__ __forceinline__ void tc_st16(uint32_t taddr, const float (&v)[16]) {
           "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
         : "memory");
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 // generic-proxy writes to shared memory visible to the tensor cores
 __device__ __forceinline__ void tc_fence_async_smem() {

@@ -1,10 +1,12 @@
-// Library runtime: last-error text, version, stream check, and the device
-// error word that kernels set instead of touching an out-of-range address.
+// Library runtime: last-error text, version, stream check, the device
+// error word that kernels set instead of touching an out-of-range address
+// or waiting without end, and a self-test of the bounded in-kernel waits.
 #include <mutex>
 #include <string>
 
 #include "pagedkv.h"
 #include "pkv_device.cuh"
+#include "tc_wait.cuh"
 
 namespace {
 
@@ -23,6 +25,39 @@ int current_device() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
     return dev;
+}
+
+// The steps a tensor-core prefix CTA takes when one of its waits runs out:
+// one warp takes TMEM, waits on an mbarrier that nothing completes for
+// `polls` rounds, reports PKV_DEVERR_TIMEOUT, frees the TMEM and returns.
+__global__ void __launch_bounds__(32, 1) wait_selftest_kernel(int* err, long long polls) {
+    __shared__ __align__(8) unsigned long long bar;
+    __shared__ uint32_t tslot;
+    __shared__ int abort_flag;
+    const uint32_t b = (uint32_t)__cvta_generic_to_shared(&bar);
+    const int lane = threadIdx.x & 31;
+    if (lane == 0) {
+        tc_mbar_init(b, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        abort_flag = 0;
+    }
+    __syncwarp();
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 32;"
+                 ::"r"((uint32_t)__cvta_generic_to_shared(&tslot))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tc_fence_before();
+    __syncwarp();
+    tc_fence_after();
+    const uint32_t tmem = tslot;
+    int ok = 1;
+    if (lane == 0) ok = tc_mbar_wait(b, 0u, &abort_flag, polls) ? 1 : 0;  // nothing arrives
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok && lane == 0) pkv::report(err, PKV_DEVERR_TIMEOUT);
+    tc_fence_before();
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 32;" ::"r"(tmem) : "memory");
 }
 
 }  // namespace
@@ -92,6 +127,18 @@ pkv_status pkv_get_device_errors(int32_t* flags) {
     e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return pkv::cuda_fail(e, "get_device_errors");
     *flags = v;
+    return PKV_OK;
+}
+
+pkv_status pkv_selftest_bounded_wait(int64_t polls, void* stream) {
+    pkv::clear_error();
+    if (polls < 1 || polls > kTcWaitLimit)
+        return pkv::fail(PKV_ERR_INVALID_ARG, "selftest_bounded_wait: polls must be in [1, 2^20]");
+    int* err = pkv::device_error_word();
+    if (!err) return pkv::fail(PKV_ERR_CUDA, "selftest_bounded_wait: no device error word");
+    wait_selftest_kernel<<<1, 32, 0, pkv::as_stream(stream)>>>(err, (long long)polls);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return pkv::cuda_fail(e, "selftest_bounded_wait launch");
     return PKV_OK;
 }
 

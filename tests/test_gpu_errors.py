@@ -1,6 +1,7 @@
 """Out-of-range ids are never dereferenced: the kernels skip the access and
 set a bit in the device error word, which the host reads.  Every bad id
-below is caught by the kernels' own bounds checks."""
+below is caught by the kernels' own bounds checks.  A bounded in-kernel wait
+that runs out reports through the same word and leaves the context usable."""
 import numpy as np
 import pytest
 import torch
@@ -85,3 +86,40 @@ def test_bad_prefix_group_is_flagged_and_skipped():
     torch.cuda.synchronize()
     assert P.pkv_get_device_errors() & L.PKV_DEVERR_GROUP
     assert_attention_close(out_to_double(st.out), r["ref"].out, "bad group")
+
+
+@pytest.mark.parametrize("polls", [1, 1 << 12, 1 << 20])
+def test_bounded_wait_gives_up_reports_and_leaves_the_context_usable(polls, monkeypatch):
+    """A wait that nothing completes runs out after its bounded number of
+    polls: the kernel sets PKV_DEVERR_TIMEOUT, frees its tensor memory and
+    returns; the host reads the bit, and the next calls -- the tcgen05
+    prefix kernel, which takes tensor memory again -- run normally."""
+    import time
+    import workloads as W
+    from tests.gpu_harness import assert_attention_close, compare_step, out_to_double
+    P.pkv_get_device_errors()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    L.pkv_selftest_bounded_wait(polls)
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    assert P.pkv_get_device_errors() == L.PKV_DEVERR_TIMEOUT
+    print(f"{polls} polls gave up after {dt * 1e3:.2f} ms")
+    assert dt < 30.0
+    L.pkv_sync_check()
+    monkeypatch.setenv("PKV_PREFIX_KERNEL", "tcgen05")
+    w = W.shared_prefix(seed=5, prompts=2, samples=4, prefix=256, tail_lo=1, tail_hi=40, H=4,
+                        D=128)
+    r = compare_step(w, partition_tokens=128)
+    st = r["step"]
+    st.out.fill_(float("nan"))
+    st.decode_shared_prefix(np.array([[0, 4, 256], [4, 4, 256]], dtype=np.int32))
+    torch.cuda.synchronize()
+    assert_attention_close(out_to_double(st.out), r["ref"].out, "after a timed-out wait")
+    assert P.pkv_get_device_errors() == 0
+
+
+def test_bounded_wait_rejects_out_of_range_polls():
+    for bad in (0, -1, (1 << 20) + 1):
+        with pytest.raises(L.PkvError):
+            L.pkv_selftest_bounded_wait(bad)
