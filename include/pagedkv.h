@@ -128,8 +128,8 @@ pkv_status pkv_paged_attention_decode(
  * pkv_paged_attention_decode called in that order with the same arguments
  * (same slots, same cache contents, bit-identical output); it runs in two
  * kernels instead of four (three with prefix groups), the slot mapping,
- * cache write and the decode's work plan in one.  This fusion is this library's; the pages describe the
- * three operations, not a combined call.
+ * cache write and the decode's work plan in one.  This fusion is this
+ * library's; the pages describe the three operations, not a combined call.
  *
  *   key, value    [T][H][D] dtype: K and V of the new tokens, 16-byte aligned
  *   seq_idx, pos  [T] int32: each new token's sequence and position
