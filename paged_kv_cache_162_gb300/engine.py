@@ -107,9 +107,9 @@ def paged_attention_decode_shared_prefix(out, q, k_cache, v_cache, block_tables,
     G = prefix_groups.shape[0]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    mcl = max_context_len or MB * bs
-    need = L.pkv_decode_shared_prefix_workspace_size(S, H, D, G, mcl, partition_tokens)
-    if workspace is None or workspace.numel() < need:
+    if workspace is None:
+        mcl = max_context_len or MB * bs
+        need = L.pkv_decode_shared_prefix_workspace_size(S, H, D, G, mcl, partition_tokens)
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     L.pkv_paged_attention_decode_shared_prefix(out, q, k_cache, v_cache, block_tables,
                                                context_lens, prefix_groups, G, S, H, D, bs, NB, MB,
