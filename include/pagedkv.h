@@ -389,6 +389,52 @@ int32_t pkv_alloc_num_free(const pkv_allocator* a);
 /* Blocks held more than once (refcount > 1). */
 int32_t pkv_alloc_num_shared(const pkv_allocator* a);
 
+/* ------------------------------------------------------------------ *
+ * Beam-search step in one call ([P1] 3.3.2 share_blocks; [P2]
+ * "Copy-on-Write共享解码的显存优化原理"; [P4] "Memory Sharing与写时复制":
+ * beams share their blocks until a write diverges them).  The call is
+ * exactly this sequence of the entry points above:
+ *   1. pkv_alloc_fork(a, tables, num_blocks, S, MB, parents);
+ *   2. pkv_alloc_append_batch for one new token per sequence, after
+ *      ctx_before[s] = context_lens[parents[s]] (the old lengths): the
+ *      copy-on-write pairs of shared last blocks, new blocks at block
+ *      boundaries;
+ *   3. context_lens[s] = ctx_before[s] + 1 (host array, in place);
+ *   4. the tables, lengths, token positions (ctx_before), sequence index
+ *      (0..S-1) and copy pairs are written into `staging` and uploaded to
+ *      `dev_inputs` by one cudaMemcpyAsync on `stream`;
+ *   5. pkv_copy_blocks for the pairs, then pkv_decode_step for the S new
+ *      tokens (key/value/q [S][H][D], device) with max_context_len = MB*bs.
+ *
+ *   tables [S][MB], num_blocks [S], context_lens [S]: host int32, in place
+ *   parents [S]: host int32, each in [0, S)
+ *   staging: pinned host memory, dev_inputs: device memory, both 256-byte
+ *           aligned and inputs_bytes >= pkv_beam_inputs_bytes(S, MB) long.
+ *           The copy out of `staging` is asynchronous: the caller does not
+ *           pass the same staging buffer again before `stream` has passed
+ *           this call (two buffers used in turn, with an event, work).
+ *           dev_inputs is read by this step's kernels on `stream`, so one
+ *           device buffer serves every step on that stream.
+ *   slot_mapping [S] int64 (device, written); workspace of at least
+ *           pkv_decode_workspace_size(S, H, D, MB*bs, partition_tokens)
+ *   *n_pairs  receives the number of copy pairs; they are in `staging`
+ *           at the offset the layout gives (int64 [n][2], after the
+ *           tables, lengths, positions and sequence index)
+ * Errors: arguments are checked before step 1 (PKV_ERR_INVALID_ARG: a
+ * parent out of range, a context that would pass the table, buffers too
+ * small or misaligned).  A failure of step 1 changes nothing; a failure of
+ * step 2 (PKV_ERR_OOM) leaves the fork done and the first sequences
+ * extended, as pkv_alloc_append_batch describes, and launches nothing. */
+size_t pkv_beam_inputs_bytes(int32_t S, int32_t MB);
+
+pkv_status pkv_beam_step(
+    pkv_allocator* a, int32_t* tables, int32_t* num_blocks, int32_t* context_lens,
+    const int32_t* parents, int32_t S, int32_t MB, void* staging, void* dev_inputs,
+    size_t inputs_bytes, void* out, const void* q, const void* key, const void* value,
+    void* k_cache, void* v_cache, int64_t* slot_mapping, int H, int D, int bs, int NB,
+    float scale, pkv_dtype dtype, int partition_tokens, void* workspace,
+    size_t workspace_bytes, int32_t* n_pairs, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

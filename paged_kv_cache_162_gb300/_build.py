@@ -20,7 +20,7 @@ LIB = os.path.join(PKG, "libpagedkv.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CU_SOURCES = ["runtime.cu", "cache_ops.cu", "decode.cu"]
-CXX_SOURCES = ["allocator.cpp"]
+CXX_SOURCES = ["allocator.cpp", "beam_step.cpp"]
 
 
 def cuda_home() -> str:

@@ -27,6 +27,9 @@ struct pkv_allocator {
     int32_t shared = 0;            // blocks with rc > 1
     std::vector<int32_t> stack;    // free ids, top of stack at [top-1]
     std::vector<int32_t> rc;       // refcount per block
+    std::vector<int32_t> delta;    // fork scratch, all zero between calls
+    std::vector<int32_t> nchild;   // fork scratch: children per row
+    std::vector<int32_t> rows;     // fork scratch: the old tables
 };
 
 namespace {
@@ -62,6 +65,7 @@ pkv_status pkv_alloc_create(int32_t num_blocks, pkv_allocator** out) {
         a->num_blocks = num_blocks;
         a->stack.resize(num_blocks);
         a->rc.assign(num_blocks, 0);
+        a->delta.assign(num_blocks, 0);
     } catch (...) {
         delete a;
         return pkv::fail(PKV_ERR_INVALID_ARG, "alloc_create: out of host memory");
@@ -254,38 +258,57 @@ pkv_status pkv_alloc_fork(pkv_allocator* a, int32_t* tables, int32_t* num_blocks
                 return pkv::fail(PKV_ERR_INVALID_ARG, "alloc_fork: table holds a block that is not held");
         }
     }
-    // releases must not underflow: a block released k times by the old rows
-    // needs rc + (holds the new rows take) >= k
-    std::vector<int32_t> old_tab((size_t)S * MB), old_nb(num_blocks, num_blocks + S);
-    std::copy(tables, tables + (size_t)S * MB, old_tab.begin());
-    for (int32_t s = 0; s < S; ++s)
-        for (int32_t j = 0; j < old_nb[parents[s]]; ++j) a->rc[old_tab[(size_t)parents[s] * MB + j]] += 1;
-    for (int32_t s = 0; s < S; ++s)
-        for (int32_t j = 0; j < old_nb[s]; ++j) a->rc[old_tab[(size_t)s * MB + j]] -= 1;
+    // Row r of the old tables is copied into nchild[r] new rows, so each of
+    // its entries changes its block's count by nchild[r] - 1: rows forked
+    // once change nothing.  The counts are checked before anything changes
+    // (no release may underflow), then holds are added (rows with several
+    // children) before the releases (rows with none), in row order, so a
+    // block that survives never reaches 0 and the freed blocks reach the
+    // free list in the order the releases one by one would give.
+    try {
+        a->nchild.assign(S, 0);
+        a->rows.assign(tables, tables + (size_t)S * MB);
+    } catch (...) {
+        return pkv::fail(PKV_ERR_INVALID_ARG, "alloc_fork: out of host memory");
+    }
+    int32_t* nchild = a->nchild.data();
+    const int32_t* old_tab = a->rows.data();
+    for (int32_t s = 0; s < S; ++s) ++nchild[parents[s]];
+    int32_t* delta = a->delta.data();
+    for (int32_t r = 0; r < S; ++r) {
+        if (nchild[r] == 1) continue;
+        for (int32_t j = 0; j < num_blocks[r]; ++j) delta[old_tab[(size_t)r * MB + j]] += nchild[r] - 1;
+    }
     bool ok = true;
-    for (int32_t s = 0; s < S && ok; ++s)
-        for (int32_t j = 0; j < old_nb[s]; ++j) ok = ok && a->rc[old_tab[(size_t)s * MB + j]] >= 0;
-    // undo the probe, then apply for real through set_rc / push
-    for (int32_t s = 0; s < S; ++s)
-        for (int32_t j = 0; j < old_nb[s]; ++j) a->rc[old_tab[(size_t)s * MB + j]] += 1;
-    for (int32_t s = 0; s < S; ++s)
-        for (int32_t j = 0; j < old_nb[parents[s]]; ++j) a->rc[old_tab[(size_t)parents[s] * MB + j]] -= 1;
-    if (!ok) return pkv::fail(PKV_ERR_INVALID_ARG, "alloc_fork: release would underflow a refcount");
-    for (int32_t s = 0; s < S; ++s)
-        for (int32_t j = 0; j < old_nb[parents[s]]; ++j) {
-            const int32_t id = old_tab[(size_t)parents[s] * MB + j];
-            set_rc(a, id, a->rc[id] + 1);
+    for (int32_t r = 0; r < S; ++r) {
+        if (nchild[r] == 1) continue;
+        for (int32_t j = 0; j < num_blocks[r]; ++j) {
+            const int32_t id = old_tab[(size_t)r * MB + j];
+            ok = ok && a->rc[id] + delta[id] >= 0;
+            delta[id] = 0;
         }
-    for (int32_t s = 0; s < S; ++s)
-        for (int32_t j = 0; j < old_nb[s]; ++j) {
-            const int32_t id = old_tab[(size_t)s * MB + j];
+    }
+    if (!ok) return pkv::fail(PKV_ERR_INVALID_ARG, "alloc_fork: release would underflow a refcount");
+    for (int32_t r = 0; r < S; ++r) {
+        if (nchild[r] < 2) continue;
+        for (int32_t j = 0; j < num_blocks[r]; ++j) {
+            const int32_t id = old_tab[(size_t)r * MB + j];
+            set_rc(a, id, a->rc[id] + nchild[r] - 1);
+        }
+    }
+    for (int32_t r = 0; r < S; ++r) {
+        if (nchild[r] != 0) continue;
+        for (int32_t j = 0; j < num_blocks[r]; ++j) {
+            const int32_t id = old_tab[(size_t)r * MB + j];
             set_rc(a, id, a->rc[id] - 1);
             if (a->rc[id] == 0) push(a, id);
         }
+    }
+    std::vector<int32_t>& old_nb = a->nchild;  // children counted; reuse for the lengths
+    std::copy(num_blocks, num_blocks + S, old_nb.begin());
     for (int32_t s = 0; s < S; ++s) {
         const int32_t p = parents[s];
-        std::copy(old_tab.begin() + (size_t)p * MB, old_tab.begin() + (size_t)(p + 1) * MB,
-                  tables + (size_t)s * MB);
+        std::memcpy(tables + (size_t)s * MB, old_tab + (size_t)p * MB, (size_t)MB * 4);
         num_blocks[s] = old_nb[p];
     }
     return PKV_OK;

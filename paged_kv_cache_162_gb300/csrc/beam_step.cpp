@@ -1,0 +1,129 @@
+// One beam-search step in one native call: the host allocator's fork and
+// append, the upload of what the device needs, and the step's kernels.
+//
+//  "3.3 页面级显存管理" 3.3.2: share_blocks when a sequence forks (beam
+//    search, parallel sampling), one more block when a sequence's tokens
+//    pass num_blocks * block_size
+//  "vLLM三大核心技术分页内存与共享解码", "Copy-on-Write共享解码的显存优化原理":
+//    a write into a shared block copies it first
+//  notes on "vLLM: Easy, Fast, and Cheap LLM Serving with PagedAttention",
+//    "Memory Sharing与写时复制": beams share blocks until they diverge
+//
+// The call is the composition of public entry points -- pkv_alloc_fork,
+// pkv_alloc_append_batch, pkv_copy_blocks and pkv_decode_step -- with the
+// host arrays staged in one pinned buffer and uploaded by one copy, so a
+// serving loop crosses the library boundary once per step.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "pagedkv.h"
+#include "pkv_internal.h"
+
+namespace {
+
+// Byte offsets of the staged inputs (the same in the pinned staging buffer
+// and in the device buffer): tables [S][MB] int32, context lengths [S],
+// token positions [S], sequence index [S] (int32), copy pairs [S][2] int64.
+// Every part starts on a 256-byte boundary.
+struct BeamLayout {
+    size_t tables, ctx, pos, seq, pairs, total;
+};
+
+size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+BeamLayout beam_layout(int32_t S, int32_t MB) {
+    BeamLayout L;
+    L.tables = 0;
+    L.ctx = up256((size_t)S * MB * 4);
+    L.pos = L.ctx + up256((size_t)S * 4);
+    L.seq = L.pos + up256((size_t)S * 4);
+    L.pairs = L.seq + up256((size_t)S * 4);
+    L.total = L.pairs + up256((size_t)S * 2 * 8);
+    return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pkv_beam_inputs_bytes(int32_t S, int32_t MB) {
+    if (S <= 0 || MB <= 0) return 0;
+    return beam_layout(S, MB).total;
+}
+
+pkv_status pkv_beam_step(pkv_allocator* a, int32_t* tables, int32_t* num_blocks,
+                         int32_t* context_lens, const int32_t* parents, int32_t S, int32_t MB,
+                         void* staging, void* dev_inputs, size_t inputs_bytes, void* out,
+                         const void* q, const void* key, const void* value, void* k_cache,
+                         void* v_cache, int64_t* slot_mapping, int H, int D, int bs, int NB,
+                         float scale, pkv_dtype dtype, int partition_tokens, void* workspace,
+                         size_t workspace_bytes, int32_t* n_pairs, void* stream) {
+    pkv::clear_error();
+    if (!a || S <= 0 || MB <= 0 || !tables || !num_blocks || !context_lens || !parents ||
+        !staging || !dev_inputs || !n_pairs || bs <= 0)
+        return pkv::fail(PKV_ERR_INVALID_ARG, "beam_step: bad argument");
+    const BeamLayout L = beam_layout(S, MB);
+    if (inputs_bytes < L.total)
+        return pkv::fail(PKV_ERR_INVALID_ARG, "beam_step: staging/device input buffers too small");
+    if ((reinterpret_cast<uintptr_t>(staging) & 255u) || (reinterpret_cast<uintptr_t>(dev_inputs) & 255u))
+        return pkv::fail(PKV_ERR_INVALID_ARG, "beam_step: input buffers must be 256-byte aligned");
+    for (int32_t s = 0; s < S; ++s)
+        if (parents[s] < 0 || parents[s] >= S)
+            return pkv::fail(PKV_ERR_INVALID_ARG, "beam_step: parent out of range");
+    *n_pairs = 0;
+
+    unsigned char* stg = static_cast<unsigned char*>(staging);
+    int32_t* pos = reinterpret_cast<int32_t*>(stg + L.pos);
+    int32_t* ctx = reinterpret_cast<int32_t*>(stg + L.ctx);
+    int32_t* seq = reinterpret_cast<int32_t*>(stg + L.seq);
+    int64_t* pairs = reinterpret_cast<int64_t*>(stg + L.pairs);
+
+    // the new token of sequence s sits at its parent's old length
+    for (int32_t s = 0; s < S; ++s) {
+        pos[s] = context_lens[parents[s]];
+        if (pos[s] < 0 || pos[s] >= MB * bs)
+            return pkv::fail(PKV_ERR_INVALID_ARG, "beam_step: a context would pass the table");
+    }
+    pkv_status st = pkv_alloc_fork(a, tables, num_blocks, S, MB, parents);
+    if (st != PKV_OK) return st;
+    // one token per sequence: seq doubles as the n_new array (all ones)
+    for (int32_t s = 0; s < S; ++s) seq[s] = 1;
+    int32_t np = 0, ndone = 0;
+    st = pkv_alloc_append_batch(a, tables, num_blocks, S, MB, pos, seq, bs, pairs, 2 * S, &np,
+                                &ndone);
+    if (st != PKV_OK) return st;  // forked; rows [0, ndone) extended, nothing launched
+    for (int32_t s = 0; s < S; ++s) {
+        context_lens[s] = pos[s] + 1;
+        ctx[s] = context_lens[s];
+        seq[s] = s;
+    }
+    std::memcpy(stg + L.tables, tables, (size_t)S * MB * 4);
+    *n_pairs = np;
+
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const size_t used = np ? L.pairs + (size_t)np * 16 : L.pairs;
+    cudaError_t e = cudaMemcpyAsync(dev_inputs, staging, used, cudaMemcpyHostToDevice, cs);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return pkv::fail(PKV_ERR_CUDA, "beam_step: input upload failed");
+    }
+    unsigned char* dev = static_cast<unsigned char*>(dev_inputs);
+    if (np) {
+        st = pkv_copy_blocks(k_cache, v_cache, reinterpret_cast<const int64_t*>(dev + L.pairs), np,
+                             H, D, bs, NB, dtype, stream);
+        if (st != PKV_OK) return st;
+    }
+    // max_context_len 0: the workspace is sized for MB * bs, so it serves
+    // every step of the search
+    return pkv_decode_step(out, q, key, value, k_cache, v_cache,
+                           reinterpret_cast<const int32_t*>(dev + L.tables),
+                           reinterpret_cast<const int32_t*>(dev + L.ctx),
+                           reinterpret_cast<const int32_t*>(dev + L.seq),
+                           reinterpret_cast<const int32_t*>(dev + L.pos), slot_mapping, nullptr, 0,
+                           S, S, H, D, bs, NB, MB, 0, scale, dtype, partition_tokens, workspace,
+                           workspace_bytes, stream);
+}
+
+}  // extern "C"

@@ -216,7 +216,10 @@ class DecodeStep:
         self.prefix_groups = None
 
     def plan(self):
-        """Host allocator: tables and copy-on-write pairs for this step."""
+        """Host allocator: tables and copy-on-write pairs for this step.
+        A new plan also starts a new beam search (beam_step)."""
+        for name in ("beam_ctx", "_beam_args"):
+            self.__dict__.pop(name, None)
         self.allocator = BlockAllocator(self.NB, self.initial_free)
         ids, counts = np.unique(self.tables_pre[self.tables_pre >= 0], return_counts=True)
         for b, c in zip(ids.tolist(), counts.tolist()):
@@ -261,113 +264,114 @@ class DecodeStep:
         return self.out
 
     def _beam_buffers(self):
-        """Two pinned staging slots (int32 ints, int64 pairs, 16-bit tokens)
-        and their device twins, so each step uploads with three async
-        copies; an event per slot keeps a slot from being overwritten while
-        its copy may still be in flight."""
+        """Buffers of the native beam step: two pinned staging buffers used
+        in turn (an event per buffer keeps one from being rewritten while
+        its upload may still be in flight), the device twin they upload to,
+        a device buffer for host-given tokens, and a workspace sized for
+        the longest context the tables allow."""
         S, MB, H, D = self.S, self.MB, self.H, self.D
-        n32 = S * MB + 2 * S
-        n64 = 2 * 2 * S          # at most 2 copies per sequence and step
-        n16 = 3 * S * H * D
         dev = self.device
+        nb = L.pkv_beam_inputs_bytes(S, MB)
+        self._beam_inputs_bytes = nb
         self._beam_slots = []
         for _ in range(2):
-            self._beam_slots.append({
-                "i32": torch.empty(n32, dtype=torch.int32).pin_memory(),
-                "i64": torch.empty(n64, dtype=torch.int64).pin_memory(),
-                "u16": torch.empty(n16, dtype=torch.int16).pin_memory(),
-                "done": None})
-        self._beam_dev = {"i32": torch.empty(n32, dtype=torch.int32, device=dev),
-                          "i64": torch.empty(n64, dtype=torch.int64, device=dev),
-                          "u16": torch.empty(n16, dtype=torch.int16, device=dev)}
+            raw = torch.empty(nb + 256, dtype=torch.uint8).pin_memory()
+            off = (-raw.data_ptr()) % 256
+            stg = raw[off:off + nb]
+            self._beam_slots.append({"stg": stg, "stg_np": stg.numpy(),
+                                     "u16": torch.empty(3 * S * H * D, dtype=torch.int16).pin_memory(),
+                                     "done": torch.cuda.Event(), "used": False})
+        self._beam_dev_inputs = torch.empty(nb, dtype=torch.uint8, device=dev)
+        self._beam_dev_u16 = torch.empty(3 * S * H * D, dtype=torch.int16, device=dev)
         self._beam_turn = 0
+        self._beam_ws = new_workspace(S, H, D, MB * self.bs, self.partition_tokens, dev)
+        # decode() after beam steps: the tables allow contexts up to MB * bs
+        self.workspace, self.max_context_len = self._beam_ws, MB * self.bs
         if self.slot_mapping.numel() < S:
             self.slot_mapping = torch.empty(S, dtype=torch.int64, device=dev)
+        # offsets of the staged inputs (the layout pkv_beam_step documents)
+        up = lambda x: (x + 255) // 256 * 256
+        o_ctx = up(4 * S * MB)
+        o_pos = o_ctx + up(4 * S)
+        o_seq = o_pos + up(4 * S)
+        self._beam_offsets = {"ctx": o_ctx, "pos": o_pos, "seq": o_seq, "pairs": o_seq + up(4 * S)}
+        self._beam_npairs = ctypes.c_int32(0)
+        # the step's device inputs, as views of the uploaded buffer
+        d = self._beam_dev_inputs
+        self._beam_views = (d[:4 * S * MB].view(torch.int32).view(S, MB),
+                            d[o_ctx:o_ctx + 4 * S].view(torch.int32),
+                            d[o_pos:o_pos + 4 * S].view(torch.int32),
+                            d[o_seq:o_seq + 4 * S].view(torch.int32))
 
     def beam_step(self, parents, new_k, new_v, q, stream=None):
         """One beam-search step after plan(): every sequence b continues from
         sequence parents[b] (fork: share the parent's blocks), appends one
         token (copy-on-write of its shared partial block first), then the
-        device copies, writes and attends.  new_k/new_v/q: [S, H, D] 16-bit
-        values, either host arrays of uint16 bit patterns (staged and
-        uploaded with the tables) or device tensors (used in place, as a
-        model on the device would produce them).  Returns the (src, dst)
-        copy pairs of the step."""
+        device copies, writes and attends -- one native call
+        (pkv_beam_step).  new_k/new_v/q: [S, H, D] 16-bit values, either
+        host arrays of uint16 bit patterns (uploaded first) or device
+        tensors (used in place, as a model on the device would produce
+        them).  Returns the (src, dst) copy pairs of the step."""
         S, MB, H, D, bs = self.S, self.MB, self.H, self.D, self.bs
         if not hasattr(self, "beam_ctx"):
-            self.beam_ctx = self.context_lens_host.astype(np.int32).copy()
+            self.beam_ctx = np.ascontiguousarray(self.context_lens_host, dtype=np.int32).copy()
             self.nblocks_host = np.ascontiguousarray(self.nblocks_host, dtype=np.int32)
+            self.tables_host = np.ascontiguousarray(self.tables_host, dtype=np.int32)
             self._beam_buffers()
-        # host: fork (share the parents' blocks) and append, two native calls
-        t0 = time.perf_counter()
-        parents = np.asarray(parents, dtype=np.int64)
-        self.allocator.fork(self.tables_host, self.nblocks_host, parents)
-        ctx = self.beam_ctx[parents]
-        pairs = self.allocator.append_batch(self.tables_host, self.nblocks_host, ctx,
-                                            np.ones(S, dtype=np.int32), bs)
-        self.last_allocator_seconds = time.perf_counter() - t0
-        self.beam_ctx = ctx + 1
-        self.pairs_host = pairs
-        self.context_lens_host = self.beam_ctx
-        self.max_context_len = max(int(self.beam_ctx.max()), 1)
-        P = len(pairs)
-        # stage in pinned memory, then three async copies on the stream
+        st = stream if stream is not None else torch.cuda.current_stream()
         slot = self._beam_slots[self._beam_turn]
         self._beam_turn ^= 1
-        if slot["done"] is not None:
+        if slot["used"]:
             slot["done"].synchronize()
-        i32 = slot["i32"].numpy()
-        i32[:S * MB] = self.tables_host.ravel()
-        i32[S * MB:S * MB + S] = self.beam_ctx
-        i32[S * MB + S:] = ctx
-        if P:
-            slot["i64"].numpy()[:2 * P] = pairs.ravel()
         n = S * H * D
         on_device = all(isinstance(t, torch.Tensor) and t.is_cuda for t in (q, new_k, new_v))
-        if not on_device:
+        if on_device:
+            for t in (q, new_k, new_v):
+                if t.element_size() != 2 or t.numel() != n or not t.is_contiguous():
+                    raise L.PkvError(L.PKV_ERR_INVALID_ARG,
+                                     "beam_step: q/new_k/new_v must be contiguous [S, H, D] 16-bit")
+            tq, tk, tv = q, new_k, new_v
+        else:
             u16 = slot["u16"].numpy().view(np.uint16)
             u16[:n] = np.asarray(q).ravel()
             u16[n:2 * n] = np.asarray(new_k).ravel()
             u16[2 * n:] = np.asarray(new_v).ravel()
-        st = stream if stream is not None else torch.cuda.current_stream()
-        d = self._beam_dev
-        with torch.cuda.stream(st):
-            d["i32"].copy_(slot["i32"], non_blocking=True)
-            if P:
-                d["i64"][:2 * P].copy_(slot["i64"][:2 * P], non_blocking=True)
-            if not on_device:
-                d["u16"].copy_(slot["u16"], non_blocking=True)
-            ev = torch.cuda.Event()
-            ev.record(st)
-        slot["done"] = ev
-        self.block_tables = d["i32"][:S * MB].view(S, MB)
-        self.context_lens = d["i32"][S * MB:S * MB + S]
-        self.pos = d["i32"][S * MB + S:S * MB + 2 * S]
-        if getattr(self, "_beam_seq_idx", None) is None:
-            self._beam_seq_idx = torch.arange(S, dtype=torch.int32, device=self.device)
-        self.seq_idx = self._beam_seq_idx
-        if on_device:
-            def as_tokens(t):
-                if t.element_size() != 2 or t.numel() != n or not t.is_contiguous():
-                    raise L.PkvError(L.PKV_ERR_INVALID_ARG,
-                                     "beam_step: q/new_k/new_v must be contiguous [S, H, D] 16-bit")
-                return t.view(self.dtype).view(S, H, D)
-            self.q, self.new_k, self.new_v = as_tokens(q), as_tokens(new_k), as_tokens(new_v)
-        else:
-            tok = d["u16"].view(self.dtype)
-            self.q = tok[:n].view(S, H, D)
-            self.new_k = tok[n:2 * n].view(S, H, D)
-            self.new_v = tok[2 * n:].view(S, H, D)
+            with torch.cuda.stream(st):
+                self._beam_dev_u16.copy_(slot["u16"], non_blocking=True)
+            tok = self._beam_dev_u16.view(self.dtype)
+            tq, tk, tv = (tok[:n].view(S, H, D), tok[n:2 * n].view(S, H, D),
+                          tok[2 * n:].view(S, H, D))
+        par = np.ascontiguousarray(parents, dtype=np.int32)
+        if getattr(self, "_beam_args", None) is None:
+            # the pointers that stay the same from step to step
+            self._beam_args = (
+                self.allocator._h, self.tables_host.ctypes.data, self.nblocks_host.ctypes.data,
+                self.beam_ctx.ctypes.data, self._beam_dev_inputs.data_ptr(),
+                self._beam_inputs_bytes, self.out.data_ptr(), self.k_cache.data_ptr(),
+                self.v_cache.data_ptr(), self.slot_mapping.data_ptr(), self._beam_ws.data_ptr(),
+                self._beam_ws.numel(), ctypes.addressof(self._beam_npairs))
+        h, p_tab, p_nb, p_ctx, p_dev, nbytes, p_out, p_k, p_v, p_slot, p_ws, ws_n, p_n = \
+            self._beam_args
+        t0 = time.perf_counter()
+        status = L.lib().pkv_beam_step(
+            h, p_tab, p_nb, p_ctx, par.ctypes.data, S, MB, slot["stg"].data_ptr(), p_dev, nbytes,
+            p_out, tq.data_ptr(), tk.data_ptr(), tv.data_ptr(), p_k, p_v, p_slot, H, D, bs,
+            self.NB, self.scale, dtype_code(self.dtype), self.partition_tokens, p_ws, ws_n, p_n,
+            st.cuda_stream)
+        self.last_native_seconds = time.perf_counter() - t0
+        L.check(status, "beam_step")
+        P = self._beam_npairs.value
+        slot["done"].record(st)
+        slot["used"] = True
+        o = self._beam_offsets["pairs"]
+        pairs = (slot["stg_np"][o:o + 16 * P].view(np.int64).reshape(P, 2).copy() if P
+                 else np.empty((0, 2), dtype=np.int64))
+        self.pairs_host = pairs
+        self.context_lens_host = self.beam_ctx
         self.T = S
-        need = workspace_size(S, H, D, self.max_context_len, self.partition_tokens)
-        if self.workspace.numel() < need:
-            self.workspace = torch.empty(need, dtype=torch.uint8, device=self.device)
-        if P:
-            self.pairs = d["i64"][:2 * P].view(P, 2)
-            copy_blocks(self.k_cache, self.v_cache, self.pairs, st)
-        compute_slot_mapping(self.slot_mapping, self.block_tables, self.seq_idx, self.pos, bs, st)
-        reshape_and_cache(self.new_k, self.new_v, self.k_cache, self.v_cache, self.slot_mapping, st)
-        self.decode(st)
+        self.q, self.new_k, self.new_v = tq, tk, tv
+        (self.block_tables, self.context_lens, self.pos,
+         self.seq_idx) = self._beam_views
         return pairs
 
     def pack_inputs(self):

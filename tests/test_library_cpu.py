@@ -297,3 +297,93 @@ def test_library_fork_and_append_batch_errors():
         a.append_batch(t, nb, [20, 20], [40, 40], 16)
     assert nb.tolist() == [4, 2] and a.num_free == 1
     assert t[1, :2].tolist() == t[0, :1].tolist() + [t[1, 1]] and t[1, 2] == -1
+
+
+def test_beam_inputs_layout():
+    """pkv_beam_inputs_bytes: tables, lengths, positions and sequence index
+    (int32) and up to 2 int64 words of copy pair per sequence, each part
+    on a 256-byte boundary."""
+    up = lambda x: (x + 255) // 256 * 256
+    for S, MB in [(1, 1), (64, 66), (7, 13), (256, 128)]:
+        want = up(4 * S * MB) + 3 * up(4 * S) + up(16 * S)
+        assert L.pkv_beam_inputs_bytes(S, MB) == want
+    assert L.pkv_beam_inputs_bytes(0, 4) == 0 and L.pkv_beam_inputs_bytes(4, 0) == 0
+
+
+def test_beam_step_rejects_bad_calls_before_changing_anything():
+    """Every argument check of pkv_beam_step runs before the fork: a bad
+    call leaves tables, lengths and refcounts as they were (no GPU needed,
+    nothing is launched)."""
+    S, MB, bs = 4, 4, 16
+    a = BlockAllocator(32)
+    ids = a.alloc(2)
+    a.incref([ids[0], ids[0], ids[0], ids[1], ids[1], ids[1]])
+    tables = np.full((S, MB), -1, dtype=np.int32)
+    tables[:, 0], tables[:, 1] = ids[0], ids[1]
+    nb = np.full(S, 2, dtype=np.int32)
+    ctx = np.full(S, 20, dtype=np.int32)
+    nbytes = L.pkv_beam_inputs_bytes(S, MB)
+    stg = np.zeros(nbytes + 512, dtype=np.uint8)
+    base = stg.ctypes.data
+    aligned = base + (-base) % 256
+    fake_dev = 1 << 20  # 256-byte aligned; never reached by these calls
+
+    def call(parents, staging=aligned, inputs_bytes=nbytes, context=ctx):
+        return L.lib().pkv_beam_step(a._h, tables.ctypes.data, nb.ctypes.data, context.ctypes.data,
+                                     np.ascontiguousarray(parents, dtype=np.int32).ctypes.data,
+                                     S, MB, staging, fake_dev, inputs_bytes, 0, 0, 0, 0, 0, 0, 0,
+                                     4, 64, bs, 32, 0.125, L.PKV_F16, 0, 0, 0,
+                                     ctypes.addressof(ctypes.c_int32()), 0)
+
+    before = (tables.copy(), nb.copy(), ctx.copy(), [a.refcount(i) for i in ids], a.num_free)
+    full = np.full(S, MB * bs, dtype=np.int32)
+    for status, kw in [
+        (call([0, 1, 2, 4]), "parent out of range"),
+        (call([0, -1, 2, 3]), "negative parent"),
+        (call([0, 1, 2, 3], staging=aligned + 16), "misaligned staging"),
+        (call([0, 1, 2, 3], inputs_bytes=nbytes - 1), "buffers too small"),
+        (call([0, 1, 2, 3], context=full), "context would pass the table"),
+    ]:
+        assert status == L.PKV_ERR_INVALID_ARG, kw
+        assert np.array_equal(tables, before[0]) and np.array_equal(nb, before[1]), kw
+        assert np.array_equal(ctx, before[2]), kw
+        assert [a.refcount(i) for i in ids] == before[3] and a.num_free == before[4], kw
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_library_fork_random_parents_match_model(seed):
+    """Forks with parents drawn from every row (rows with no child, one
+    child and many, shared and private blocks, ragged lengths) followed by
+    appends of 1..20 tokens: tables, copy pairs, every refcount and the free
+    list order (seen through the next allocations) equal the model's."""
+    from oracle.allocator import fork_tables as model_fork
+    rng = np.random.default_rng(seed)
+    NB, bs, S, MB = 3000, 8, 12, 200
+    lib_a, mod_a = BlockAllocator(NB), BlockAllocatorModel(NB)
+    ctx = rng.integers(1, 60, size=S).astype(np.int64)
+    tm = [[] for _ in range(S)]
+    for s in range(S):
+        mod_a.append(tm[s], 0, int(ctx[s]), bs)
+    tl = np.full((S, MB), -1, dtype=np.int32)
+    nbl = np.zeros(S, dtype=np.int32)
+    lib_a.append_batch(tl, nbl, np.zeros(S), ctx, bs)
+    for step in range(60):
+        parents = rng.integers(0, S, size=S)
+        if step % 5 == 0:
+            parents[:] = rng.integers(0, S)  # one row takes over every sequence
+        tm = model_fork(mod_a, tm, parents)
+        lib_a.fork(tl, nbl, parents)
+        ctx = ctx[parents]
+        n_new = rng.integers(1, 21, size=S)
+        pm = []
+        for s in range(S):
+            pm += mod_a.append(tm[s], int(ctx[s]), int(n_new[s]), bs)
+        pl = lib_a.append_batch(tl, nbl, ctx, n_new, bs)
+        assert [tuple(p) for p in pl.tolist()] == pm, step
+        ctx = ctx + n_new
+        for s in range(S):
+            assert tl[s, :nbl[s]].tolist() == tm[s], (step, s)
+        assert lib_a.num_free == mod_a.num_free and lib_a.num_shared == mod_a.num_shared
+        assert all(lib_a.refcount(b) == mod_a.refcount(b) for b in range(NB)), step
+    assert ctx.max() <= MB * bs
+    assert list(lib_a.alloc(50)) == list(mod_a.alloc(50))  # the free lists agree in order
