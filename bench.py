@@ -48,7 +48,8 @@ def parse_args(argv=None):
     p.add_argument("--workload", default="llama7b_batch64")
     p.add_argument("--partition-tokens", type=int, default=0)
     p.add_argument("--shared-prefix", action="store_true",
-                   help="shared_prefix workloads: decode with each prompt's prefix read once")
+                   help="shared_prefix workloads (and --measure beam_search): decode with each "
+                        "prompt's prefix read once")
     p.add_argument("--block-size", type=int, default=0,
                    help="llama7b_batch64 only: another block size (8, 16, 32, 64)")
     p.add_argument("--e2e-steps", type=int, default=200)
@@ -627,6 +628,10 @@ def run_beam(args):
                     new_v=w.new_v, seq_idx=w.seq_idx, pos=w.pos,
                     fill_bits=int(W.POISON[w.dtype]))
     st.plan()
+    if args.shared_prefix:
+        # each request's beams as a prefix group over the prompt's full blocks
+        plen = w.notes["prompt_len"]
+        st.beam_groups = [[r * bw.beams, bw.beams, (p // w.bs) * w.bs] for r, p in enumerate(plen)]
     # each step's q and new K/V on the device, as the model would produce them
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
     new_k, new_v, q = dev(bw.new_k), dev(bw.new_v), dev(bw.q)
@@ -655,6 +660,9 @@ def run_beam(args):
         "copy_pairs_per_step": float(np.mean(pairs[warm])),
         "logical_kv_gbs": float(np.mean(kv[warm])) / (wall_ms * 1e-3) / 1e9,
         "config": {"requests": 16, "beams": 4, "heads": w.H, "head_dim": w.D,
+                   "step_calls": "pkv_beam_step" + (" with a prefix group per request (its beams,"
+                                                    " the prompt's full blocks)"
+                                                    if args.shared_prefix else ""),
                    "block_size": w.bs, "prompt_tokens": "U{256..1024}", "steps": steps,
                    "timed_steps": steps - 4,
                    "inputs": "q and new K/V device-resident; tables, context lengths, "

@@ -404,7 +404,12 @@ int32_t pkv_alloc_num_shared(const pkv_allocator* a);
  *      (0..S-1) and copy pairs are written into `staging` and uploaded to
  *      `dev_inputs` by one cudaMemcpyAsync on `stream`;
  *   5. pkv_copy_blocks for the pairs, then pkv_decode_step for the S new
- *      tokens (key/value/q [S][H][D], device) with max_context_len = MB*bs.
+ *      tokens (key/value/q [S][H][D], device) with max_context_len = MB*bs
+ *      and the G prefix groups (device [G][3], as pkv_decode_step takes
+ *      them; G = 0: none).  The beams of one request keep their prompt's
+ *      full blocks shared for the whole search (only the ends of the
+ *      contexts are written), so a group per request -- its beams, the
+ *      prompt's full blocks as the prefix -- reads each prompt once.
  *
  *   tables [S][MB], num_blocks [S], context_lens [S]: host int32, in place
  *   parents [S]: host int32, each in [0, S)
@@ -416,7 +421,9 @@ int32_t pkv_alloc_num_shared(const pkv_allocator* a);
  *           dev_inputs is read by this step's kernels on `stream`, so one
  *           device buffer serves every step on that stream.
  *   slot_mapping [S] int64 (device, written); workspace of at least
- *           pkv_decode_workspace_size(S, H, D, MB*bs, partition_tokens)
+ *           pkv_decode_workspace_size(S, H, D, MB*bs, partition_tokens),
+ *           or with G > 0 pkv_decode_shared_prefix_workspace_size(S, H, D,
+ *           G, MB*bs, partition_tokens)
  *   *n_pairs  receives the number of copy pairs; they are in `staging`
  *           at the offset the layout gives (int64 [n][2], after the
  *           tables, lengths, positions and sequence index)
@@ -431,9 +438,9 @@ pkv_status pkv_beam_step(
     pkv_allocator* a, int32_t* tables, int32_t* num_blocks, int32_t* context_lens,
     const int32_t* parents, int32_t S, int32_t MB, void* staging, void* dev_inputs,
     size_t inputs_bytes, void* out, const void* q, const void* key, const void* value,
-    void* k_cache, void* v_cache, int64_t* slot_mapping, int H, int D, int bs, int NB,
-    float scale, pkv_dtype dtype, int partition_tokens, void* workspace,
-    size_t workspace_bytes, int32_t* n_pairs, void* stream);
+    void* k_cache, void* v_cache, int64_t* slot_mapping, const int32_t* prefix_groups, int G,
+    int H, int D, int bs, int NB, float scale, pkv_dtype dtype, int partition_tokens,
+    void* workspace, size_t workspace_bytes, int32_t* n_pairs, void* stream);
 
 #ifdef __cplusplus
 }

@@ -90,7 +90,7 @@ SIGNATURES = {
     "pkv_alloc_num_shared": (_I32, [_P]),
     "pkv_beam_inputs_bytes": (_SZ, [_I32, _I32]),
     "pkv_beam_step": (_I, [_P, _P, _P, _P, _P, _I32, _I32, _P, _P, _SZ, _P, _P, _P, _P, _P, _P,
-                           _P, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P, _P]),
+                           _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P, _P]),
 }
 
 _lib = None
@@ -242,18 +242,18 @@ def pkv_beam_inputs_bytes(S: int, MB: int) -> int:
 
 
 def pkv_beam_step(alloc_handle, tables, num_blocks, context_lens, parents, S, MB, staging,
-                  dev_inputs, inputs_bytes, out, q, key, value, k_cache, v_cache, slot_mapping, H,
-                  D, bs, NB, scale, dtype, partition_tokens, workspace, workspace_bytes,
-                  stream=None) -> int:
+                  dev_inputs, inputs_bytes, out, q, key, value, k_cache, v_cache, slot_mapping,
+                  prefix_groups, G, H, D, bs, NB, scale, dtype, partition_tokens, workspace,
+                  workspace_bytes, stream=None) -> int:
     """One beam-search step (fork, append, upload, copy_blocks, decode step);
     returns the number of copy pairs."""
     n = ctypes.c_int32(0)
     check(lib().pkv_beam_step(
         alloc_handle, ptr(tables), ptr(num_blocks), ptr(context_lens), ptr(parents), S, MB,
         ptr(staging), ptr(dev_inputs), inputs_bytes, ptr(out), ptr(q), ptr(key), ptr(value),
-        ptr(k_cache), ptr(v_cache), ptr(slot_mapping), H, D, bs, NB, float(scale), int(dtype),
-        partition_tokens, ptr(workspace), workspace_bytes, ctypes.addressof(n),
-        stream_handle(stream)), "beam_step")
+        ptr(k_cache), ptr(v_cache), ptr(slot_mapping), ptr(prefix_groups), G, H, D, bs, NB,
+        float(scale), int(dtype), partition_tokens, ptr(workspace), workspace_bytes,
+        ctypes.addressof(n), stream_handle(stream)), "beam_step")
     return int(n.value)
 
 

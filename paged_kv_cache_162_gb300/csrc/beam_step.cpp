@@ -57,12 +57,13 @@ pkv_status pkv_beam_step(pkv_allocator* a, int32_t* tables, int32_t* num_blocks,
                          int32_t* context_lens, const int32_t* parents, int32_t S, int32_t MB,
                          void* staging, void* dev_inputs, size_t inputs_bytes, void* out,
                          const void* q, const void* key, const void* value, void* k_cache,
-                         void* v_cache, int64_t* slot_mapping, int H, int D, int bs, int NB,
+                         void* v_cache, int64_t* slot_mapping, const int32_t* prefix_groups,
+                         int G, int H, int D, int bs, int NB,
                          float scale, pkv_dtype dtype, int partition_tokens, void* workspace,
                          size_t workspace_bytes, int32_t* n_pairs, void* stream) {
     pkv::clear_error();
     if (!a || S <= 0 || MB <= 0 || !tables || !num_blocks || !context_lens || !parents ||
-        !staging || !dev_inputs || !n_pairs || bs <= 0)
+        !staging || !dev_inputs || !n_pairs || bs <= 0 || G < 0 || (G > 0 && !prefix_groups))
         return pkv::fail(PKV_ERR_INVALID_ARG, "beam_step: bad argument");
     const BeamLayout L = beam_layout(S, MB);
     if (inputs_bytes < L.total)
@@ -116,13 +117,17 @@ pkv_status pkv_beam_step(pkv_allocator* a, int32_t* tables, int32_t* num_blocks,
         if (st != PKV_OK) return st;
     }
     // max_context_len 0: the workspace is sized for MB * bs, so it serves
-    // every step of the search
+    // every step of the search.  With prefix groups (the beams of one
+    // request share their prompt's full blocks for the whole search: only
+    // the ends of the contexts are ever written) each prompt is read once
+    // per request.
     return pkv_decode_step(out, q, key, value, k_cache, v_cache,
                            reinterpret_cast<const int32_t*>(dev + L.tables),
                            reinterpret_cast<const int32_t*>(dev + L.ctx),
                            reinterpret_cast<const int32_t*>(dev + L.seq),
-                           reinterpret_cast<const int32_t*>(dev + L.pos), slot_mapping, nullptr, 0,
-                           S, S, H, D, bs, NB, MB, 0, scale, dtype, partition_tokens, workspace,
+                           reinterpret_cast<const int32_t*>(dev + L.pos), slot_mapping,
+                           prefix_groups, G, S, S, H, D, bs, NB, MB, 0, scale, dtype,
+                           partition_tokens, workspace,
                            workspace_bytes, stream);
 }
 

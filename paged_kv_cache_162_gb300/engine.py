@@ -284,9 +284,27 @@ class DecodeStep:
         self._beam_dev_inputs = torch.empty(nb, dtype=torch.uint8, device=dev)
         self._beam_dev_u16 = torch.empty(3 * S * H * D, dtype=torch.int16, device=dev)
         self._beam_turn = 0
-        self._beam_ws = new_workspace(S, H, D, MB * self.bs, self.partition_tokens, dev)
+        # prefix groups ([G, 3]: first sequence, members, prefix tokens) set
+        # before the first beam_step as `beam_groups`: the beams of a
+        # request keep their prompt's full blocks shared, so each group's
+        # prefix is read once per step
+        groups = getattr(self, "beam_groups", None)
+        if groups is not None and len(groups):
+            g = np.ascontiguousarray(groups, dtype=np.int32).reshape(-1, 3)
+            self._beam_groups_dev = torch.from_numpy(g).to(dev)
+            self._beam_G = int(g.shape[0])
+            nws = L.pkv_decode_shared_prefix_workspace_size(S, H, D, self._beam_G, MB * self.bs,
+                                                            self.partition_tokens)
+            self._beam_ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+        else:
+            self._beam_groups_dev, self._beam_G = None, 0
+            self._beam_ws = new_workspace(S, H, D, MB * self.bs, self.partition_tokens, dev)
         # decode() after beam steps: the tables allow contexts up to MB * bs
-        self.workspace, self.max_context_len = self._beam_ws, MB * self.bs
+        self.max_context_len = MB * self.bs
+        if self._beam_G == 0:
+            self.workspace = self._beam_ws
+        else:
+            self.workspace = new_workspace(S, H, D, MB * self.bs, self.partition_tokens, dev)
         if self.slot_mapping.numel() < S:
             self.slot_mapping = torch.empty(S, dtype=torch.int64, device=dev)
         # offsets of the staged inputs (the layout pkv_beam_step documents)
@@ -348,16 +366,18 @@ class DecodeStep:
                 self.allocator._h, self.tables_host.ctypes.data, self.nblocks_host.ctypes.data,
                 self.beam_ctx.ctypes.data, self._beam_dev_inputs.data_ptr(),
                 self._beam_inputs_bytes, self.out.data_ptr(), self.k_cache.data_ptr(),
-                self.v_cache.data_ptr(), self.slot_mapping.data_ptr(), self._beam_ws.data_ptr(),
-                self._beam_ws.numel(), ctypes.addressof(self._beam_npairs))
-        h, p_tab, p_nb, p_ctx, p_dev, nbytes, p_out, p_k, p_v, p_slot, p_ws, ws_n, p_n = \
-            self._beam_args
+                self.v_cache.data_ptr(), self.slot_mapping.data_ptr(),
+                None if self._beam_groups_dev is None else self._beam_groups_dev.data_ptr(),
+                self._beam_G, self._beam_ws.data_ptr(), self._beam_ws.numel(),
+                ctypes.addressof(self._beam_npairs))
+        (h, p_tab, p_nb, p_ctx, p_dev, nbytes, p_out, p_k, p_v, p_slot, p_grp, G, p_ws, ws_n,
+         p_n) = self._beam_args
         t0 = time.perf_counter()
         status = L.lib().pkv_beam_step(
             h, p_tab, p_nb, p_ctx, par.ctypes.data, S, MB, slot["stg"].data_ptr(), p_dev, nbytes,
-            p_out, tq.data_ptr(), tk.data_ptr(), tv.data_ptr(), p_k, p_v, p_slot, H, D, bs,
-            self.NB, self.scale, dtype_code(self.dtype), self.partition_tokens, p_ws, ws_n, p_n,
-            st.cuda_stream)
+            p_out, tq.data_ptr(), tk.data_ptr(), tv.data_ptr(), p_k, p_v, p_slot, p_grp, G, H, D,
+            bs, self.NB, self.scale, dtype_code(self.dtype), self.partition_tokens, p_ws, ws_n,
+            p_n, st.cuda_stream)
         self.last_native_seconds = time.perf_counter() - t0
         L.check(status, "beam_step")
         P = self._beam_npairs.value

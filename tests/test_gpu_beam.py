@@ -12,12 +12,20 @@ from tests.gpu_harness import assert_attention_close, device_step
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("bs,device_tokens", [(16, False), (8, False), (16, True)])
-def test_beam_search_steps_match_oracle(bs, device_tokens):
-    bw = W.beam_search(seed=7 + bs, requests=3, beams=4, prompt_lo=20, prompt_hi=70, steps=6,
-                       H=4, D=64, bs=bs)
-    st = device_step(bw.init, 32)
+@pytest.mark.parametrize("bs,device_tokens,groups,pt,prompts", [
+    (16, False, False, 32, (20, 70)), (8, False, False, 32, (20, 70)),
+    (16, True, False, 32, (20, 70)), (16, True, True, 32, (20, 70)),
+    (8, False, True, 32, (20, 70)), (16, True, True, 0, (100, 300))])
+def test_beam_search_steps_match_oracle(bs, device_tokens, groups, pt, prompts):
+    """groups: the beams of each request decode as a prefix group over
+    their prompt's full blocks, which stay shared for the whole search."""
+    bw = W.beam_search(seed=7 + bs, requests=3, beams=4, prompt_lo=prompts[0],
+                       prompt_hi=prompts[1], steps=6, H=4, D=64, bs=bs)
+    st = device_step(bw.init, pt)
     st.plan()
+    if groups:
+        plen = bw.init.notes["prompt_len"]
+        st.beam_groups = [[r * bw.beams, bw.beams, (p // bs) * bs] for r, p in enumerate(plen)]
     if device_tokens:
         # the step's q and new K/V already on the device, as a model makes them
         dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()

@@ -332,7 +332,7 @@ def test_beam_step_rejects_bad_calls_before_changing_anything():
         return L.lib().pkv_beam_step(a._h, tables.ctypes.data, nb.ctypes.data, context.ctypes.data,
                                      np.ascontiguousarray(parents, dtype=np.int32).ctypes.data,
                                      S, MB, staging, fake_dev, inputs_bytes, 0, 0, 0, 0, 0, 0, 0,
-                                     4, 64, bs, 32, 0.125, L.PKV_F16, 0, 0, 0,
+                                     0, 0, 4, 64, bs, 32, 0.125, L.PKV_F16, 0, 0, 0,
                                      ctypes.addressof(ctypes.c_int32()), 0)
 
     before = (tables.copy(), nb.copy(), ctx.copy(), [a.refcount(i) for i in ids], a.num_free)
