@@ -14,7 +14,13 @@
  * Conventions shared by every device entry point
  *  - Device pointers are caller-owned device memory; the library allocates
  *    no device memory.  Token data (q, K, V, out, key, value) is 16-bit
- *    (pkv_dtype) and every such pointer must be 16-byte aligned.
+ *    (pkv_dtype) and every such pointer must be 16-byte aligned.  q, key,
+ *    value and out may instead point to pinned host memory (cudaHostAlloc;
+ *    the GPU addresses it with the same pointer): the kernels then read the
+ *    step's tokens and write its output across the host link (on GB300 the
+ *    coherent NVLink-C2C link to the Grace CPU), which takes the place of
+ *    copying those bytes.  The caches, tables and workspace belong in
+ *    device memory: they are read many times per call.
  *  - KV cache layout ([P3] 3.1.2 "页面结构设计", 3.1.3 step 4): separate K
  *    and V caches, each [NB][bs][H][D] row-major.  Token offset o of
  *    physical block p, head h, dim d sits at ((p*bs + o)*H + h)*D + d, i.e.

@@ -394,18 +394,29 @@ class DecodeStep:
          self.seq_idx) = self._beam_views
         return pairs
 
-    def pack_inputs(self):
-        """Move the step's device inputs (q, new K/V, block tables, context
-        lengths, token positions, copy pairs) into one device buffer, at
-        256-byte aligned offsets, so that one copy uploads all of them.
+    def pack_inputs(self, on_host=()):
+        """Move the step's inputs (q, new K/V, block tables, context lengths,
+        token positions, copy pairs) into one buffer, at 256-byte aligned
+        offsets, so that one copy uploads all of them.
 
-        Returns (device buffer, pinned host buffer holding the same bytes).
-        The step's tensors become views of the device buffer; a caller
-        writes the next step's inputs into the host buffer at the same
-        offsets (`input_offsets`) and copies it over."""
+        on_host: names among "q", "new_k", "new_v" that stay in the pinned
+        host buffer, where the kernels read them directly (a GPU can address
+        pinned host memory; on GB300 the reads cross the coherent NVLink-C2C
+        link to the Grace CPU's memory).  They come first in the buffers and
+        are not part of the upload.
+
+        Returns (device buffer, pinned host buffer holding the same bytes,
+        (device view, host view) of the bytes to upload each step).  The
+        step's tensors become views of the device buffer (of the host buffer
+        for `on_host`); a caller writes the next step's inputs into the host
+        buffer at the same offsets (`input_offsets`) and uploads."""
         if self.block_tables is None:
             self.plan()
-        names = ["q", "new_k", "new_v", "block_tables", "context_lens", "seq_idx", "pos"]
+        tokens = ["q", "new_k", "new_v"]
+        if any(n not in tokens for n in on_host):
+            raise L.PkvError(L.PKV_ERR_INVALID_ARG, "pack_inputs: on_host takes q, new_k, new_v")
+        names = [n for n in tokens if n in on_host] + [n for n in tokens if n not in on_host]
+        names += ["block_tables", "context_lens", "seq_idx", "pos"]
         if self.pairs.numel():
             names.append("pairs")
         offsets, o = {}, 0
@@ -414,14 +425,29 @@ class DecodeStep:
             offsets[n] = o
             o = (o + t.numel() * t.element_size() + 255) // 256 * 256
         buf = torch.empty(max(o, 256), dtype=torch.uint8, device=self.device)
+        views = {}
         for n in names:
             t = getattr(self, n)
             nbytes = t.numel() * t.element_size()
+            views[n] = (t, nbytes)
             view = buf[offsets[n]:offsets[n] + nbytes].view(t.dtype).view(t.shape)
             view.copy_(t)
             setattr(self, n, view)
+        host = buf.cpu().pin_memory()
+        for n in on_host:
+            t, nbytes = views[n]
+            setattr(self, n, host[offsets[n]:offsets[n] + nbytes].view(t.dtype).view(t.shape))
         self.input_offsets = offsets
-        return buf, buf.cpu().pin_memory()
+        first = offsets[names[len(on_host)]]  # the first uploaded input
+        return buf, host, (buf[first:], host[first:])
+
+    def pin_output(self):
+        """The step's output goes to a pinned host tensor (returned), which
+        becomes `out`: the kernels write it there directly, so no
+        device-to-host copy follows the step."""
+        host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        self.out = host
+        return host
 
     def decode_shared_prefix(self, prefix_groups, stream=None):
         """decode() with the prefix of each group read once (see
