@@ -431,8 +431,12 @@ int32_t pkv_alloc_num_shared(const pkv_allocator* a);
  *           or with G > 0 pkv_decode_shared_prefix_workspace_size(S, H, D,
  *           G, MB*bs, partition_tokens)
  *   *n_pairs  receives the number of copy pairs; they are in `staging`
- *           at the offset the layout gives (int64 [n][2], after the
- *           tables, lengths, positions and sequence index)
+ *           as int64 [n][2].  Layout of staging and dev_inputs, each part
+ *           at a multiple of 256 bytes (r(x) rounds x up to one): tables
+ *           [S][MB] int32 at 0; context lengths [S] int32 at
+ *           o1 = r(4*S*MB); positions [S] at o2 = o1 + r(4*S); sequence
+ *           index [S] at o3 = o2 + r(4*S); copy pairs at o3 + r(4*S), room
+ *           for 2*S of them
  * Errors: arguments are checked before step 1 (PKV_ERR_INVALID_ARG: a
  * parent out of range, a context that would pass the table, buffers too
  * small or misaligned).  A failure of step 1 changes nothing; a failure of

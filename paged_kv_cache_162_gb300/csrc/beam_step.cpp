@@ -25,8 +25,10 @@ namespace {
 
 // Byte offsets of the staged inputs (the same in the pinned staging buffer
 // and in the device buffer): tables [S][MB] int32, context lengths [S],
-// token positions [S], sequence index [S] (int32), copy pairs [S][2] int64.
-// Every part starts on a 256-byte boundary.
+// token positions [S], sequence index [S] (int32), room for 2S copy pairs
+// [2S][2] int64 (one token per sequence copies at most one block, but
+// pkv_alloc_append_batch asks for room for two per sequence).  Every part
+// starts on a 256-byte boundary.
 struct BeamLayout {
     size_t tables, ctx, pos, seq, pairs, total;
 };
@@ -40,7 +42,7 @@ BeamLayout beam_layout(int32_t S, int32_t MB) {
     L.pos = L.ctx + up256((size_t)S * 4);
     L.seq = L.pos + up256((size_t)S * 4);
     L.pairs = L.seq + up256((size_t)S * 4);
-    L.total = L.pairs + up256((size_t)S * 2 * 8);
+    L.total = L.pairs + up256((size_t)S * 2 * 2 * 8);
     return L;
 }
 
@@ -84,7 +86,7 @@ pkv_status pkv_beam_step(pkv_allocator* a, int32_t* tables, int32_t* num_blocks,
     // the new token of sequence s sits at its parent's old length
     for (int32_t s = 0; s < S; ++s) {
         pos[s] = context_lens[parents[s]];
-        if (pos[s] < 0 || pos[s] >= MB * bs)
+        if (pos[s] < 0 || (int64_t)pos[s] >= (int64_t)MB * bs)
             return pkv::fail(PKV_ERR_INVALID_ARG, "beam_step: a context would pass the table");
     }
     pkv_status st = pkv_alloc_fork(a, tables, num_blocks, S, MB, parents);

@@ -301,11 +301,11 @@ def test_library_fork_and_append_batch_errors():
 
 def test_beam_inputs_layout():
     """pkv_beam_inputs_bytes: tables, lengths, positions and sequence index
-    (int32) and up to 2 int64 words of copy pair per sequence, each part
-    on a 256-byte boundary."""
+    (int32) and room for two copy pairs (2 x 2 int64) per sequence, each
+    part on a 256-byte boundary."""
     up = lambda x: (x + 255) // 256 * 256
     for S, MB in [(1, 1), (64, 66), (7, 13), (256, 128)]:
-        want = up(4 * S * MB) + 3 * up(4 * S) + up(16 * S)
+        want = up(4 * S * MB) + 3 * up(4 * S) + up(32 * S)
         assert L.pkv_beam_inputs_bytes(S, MB) == want
     assert L.pkv_beam_inputs_bytes(0, 4) == 0 and L.pkv_beam_inputs_bytes(4, 0) == 0
 
