@@ -387,3 +387,32 @@ def test_library_fork_random_parents_match_model(seed):
         assert all(lib_a.refcount(b) == mod_a.refcount(b) for b in range(NB)), step
     assert ctx.max() <= MB * bs
     assert list(lib_a.alloc(50)) == list(mod_a.alloc(50))  # the free lists agree in order
+
+
+def test_beam_step_out_of_blocks_after_the_fork():
+    """A pool too small for the appends: the fork stands, the sequences
+    before the failing one are extended, lengths are unchanged and nothing
+    is launched (the error comes before any CUDA call)."""
+    S, MB, bs = 2, 4, 16
+    a = BlockAllocator(2)
+    ids = a.alloc(2)  # pops 1, then 0
+    tables = np.full((S, MB), -1, dtype=np.int32)
+    tables[0, 0], tables[1, 0] = ids[0], ids[1]
+    nb = np.ones(S, dtype=np.int32)
+    ctx = np.full(S, bs, dtype=np.int32)  # full blocks: each append needs a new one
+    nbytes = L.pkv_beam_inputs_bytes(S, MB)
+    stg = np.zeros(nbytes + 512, dtype=np.uint8)
+    aligned = stg.ctypes.data + (-stg.ctypes.data) % 256
+    npairs = ctypes.c_int32(-1)
+    parents = np.zeros(S, dtype=np.int32)  # both continue sequence 0
+    status = L.lib().pkv_beam_step(a._h, tables.ctypes.data, nb.ctypes.data, ctx.ctypes.data,
+                                   parents.ctypes.data, S, MB, aligned, 1 << 20, nbytes, 0, 0, 0,
+                                   0, 0, 0, 0, 0, 0, 4, 64, bs, 2, 0.125, L.PKV_F16, 0, 0, 0,
+                                   ctypes.addressof(npairs), 0)
+    assert status == L.PKV_ERR_OOM
+    # fork: both rows hold sequence 0's block; sequence 1's block was freed
+    # and handed to sequence 0's append, then the pool ran dry
+    assert tables[0, :2].tolist() == [ids[0], ids[1]] and nb[0] == 2
+    assert tables[1, :1].tolist() == [ids[0]] and nb[1] == 1
+    assert ctx.tolist() == [bs, bs] and npairs.value == 0
+    assert a.refcount(ids[0]) == 2 and a.refcount(ids[1]) == 1 and a.num_free == 0
