@@ -127,6 +127,27 @@ def test_kv_bytes_formula_matches_pages():
     assert pages == c["max_pages"] and pages * g["page_size_tokens"] == c["max_tokens"]
 
 
+def test_concurrency_example_through_the_allocator_model():
+    """The pages' admission example: requests that reserve blocks for their
+    maximum length fit 7 at a time in a 1000-block pool; the 8th is refused
+    whole and takes nothing (all-or-nothing allocation)."""
+    c = _golden("kv_sizes.json")["concurrency_example"]
+    per = -(-c["max_seq_len"] // c["block_size"])
+    assert per == c["blocks_per_request"]
+    a = BlockAllocatorModel(c["pool_blocks"])
+    admitted = 0
+    while True:
+        free_before = a.num_free
+        try:
+            a.alloc(per)
+        except OutOfBlocks:
+            assert a.num_free == free_before  # nothing taken
+            break
+        admitted += 1
+    assert admitted == c["max_concurrent"]
+    assert a.num_free == c["pool_blocks"] - c["max_concurrent"] * per
+
+
 # ------------------------------------------------------------- allocator
 @pytest.mark.parametrize("trace", load_traces(), ids=lambda t: t["name"])
 def test_allocator_model_replays_page_traces(trace):
