@@ -12,7 +12,14 @@ import ctypes
 
 import numpy as np
 
-from ._lib import OutOfBlocks, check, lib  # noqa: F401  (OutOfBlocks re-exported)
+from ._lib import PKV_ERR_INVALID_ARG, OutOfBlocks, PkvError, check, lib  # noqa: F401
+
+
+def _need_i32(a: np.ndarray, what: str) -> None:
+    """Arrays the library writes in place must already be C-contiguous int32
+    (a converted copy would leave the caller's array unchanged)."""
+    if not (isinstance(a, np.ndarray) and a.dtype == np.int32 and a.flags.c_contiguous):
+        raise PkvError(PKV_ERR_INVALID_ARG, f"{what} must be a C-contiguous int32 numpy array")
 
 
 def _i32(a) -> np.ndarray:
@@ -70,7 +77,7 @@ class BlockAllocator:
     def append_row(self, row: np.ndarray, num_blocks: int, ctx_before: int, n_new: int,
                    block_size: int):
         """In place on `row` (int32, capacity len(row)); returns (num_blocks, pairs)."""
-        assert row.dtype == np.int32 and row.flags.c_contiguous
+        _need_i32(row, "row")
         nb = ctypes.c_int32(int(num_blocks))
         npairs = ctypes.c_int32(0)
         pairs = np.empty(2 * (int(n_new) // int(block_size) + 2), dtype=np.int64)
@@ -93,8 +100,8 @@ class BlockAllocator:
         """append() for every row of `tables` ([S, MB] int32, in place; nblocks
         [S] int32 in place) in one native call.  Returns the copy pairs
         [P, 2]; raises OutOfBlocks (rows before the failing one are done)."""
-        assert tables.dtype == np.int32 and tables.flags.c_contiguous
-        assert nblocks.dtype == np.int32 and nblocks.flags.c_contiguous
+        _need_i32(tables, "tables")
+        _need_i32(nblocks, "nblocks")
         S, MB = tables.shape
         cb = _i32(ctx_before)
         nn = _i32(n_new)
@@ -110,8 +117,8 @@ class BlockAllocator:
     def fork(self, tables: np.ndarray, nblocks: np.ndarray, parents) -> None:
         """Row s becomes a copy of row parents[s] (in place), sharing its
         blocks; one native call, all-or-nothing."""
-        assert tables.dtype == np.int32 and tables.flags.c_contiguous
-        assert nblocks.dtype == np.int32 and nblocks.flags.c_contiguous
+        _need_i32(tables, "tables")
+        _need_i32(nblocks, "nblocks")
         S, MB = tables.shape
         par = _i32(parents)
         check(lib().pkv_alloc_fork(self._h, tables.ctypes.data, nblocks.ctypes.data, S, MB,

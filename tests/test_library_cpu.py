@@ -416,3 +416,18 @@ def test_beam_step_out_of_blocks_after_the_fork():
     assert tables[1, :1].tolist() == [ids[0]] and nb[1] == 1
     assert ctx.tolist() == [bs, bs] and npairs.value == 0
     assert a.refcount(ids[0]) == 2 and a.refcount(ids[1]) == 1 and a.num_free == 0
+
+
+def test_in_place_arrays_must_be_int32_contiguous():
+    """fork / append_batch / append_row write the caller's arrays in place:
+    a wrong dtype or a strided view is refused, not silently copied."""
+    a = BlockAllocator(16)
+    tables = np.full((2, 4), -1, dtype=np.int32)
+    nb = np.zeros(2, dtype=np.int32)
+    with pytest.raises(L.PkvError):
+        a.fork(tables.astype(np.int64), nb, [0, 1])
+    with pytest.raises(L.PkvError):
+        a.append_batch(tables, nb.astype(np.int64), [0, 0], [1, 1], 16)
+    with pytest.raises(L.PkvError):
+        a.append_row(np.full(8, -1, dtype=np.int32)[::2], 0, 0, 1, 16)
+    assert a.num_free == 16
