@@ -441,7 +441,10 @@ int32_t pkv_alloc_num_shared(const pkv_allocator* a);
  * parent out of range, a context that would pass the table, buffers too
  * small or misaligned).  A failure of step 1 changes nothing; a failure of
  * step 2 (PKV_ERR_OOM) leaves the fork done and the first sequences
- * extended, as pkv_alloc_append_batch describes, and launches nothing. */
+ * extended, as pkv_alloc_append_batch describes, and launches nothing.  A
+ * failure in steps 4-5 (PKV_ERR_CUDA, or an argument pkv_copy_blocks or
+ * pkv_decode_step rejects) comes after steps 1-3 have updated the host
+ * arrays and the allocator. */
 size_t pkv_beam_inputs_bytes(int32_t S, int32_t MB);
 
 pkv_status pkv_beam_step(
