@@ -12,15 +12,17 @@ from tests.gpu_harness import assert_attention_close, device_step
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("bs,device_tokens,groups,pt,prompts", [
-    (16, False, False, 32, (20, 70)), (8, False, False, 32, (20, 70)),
-    (16, True, False, 32, (20, 70)), (16, True, True, 32, (20, 70)),
-    (8, False, True, 32, (20, 70)), (16, True, True, 0, (100, 300))])
-def test_beam_search_steps_match_oracle(bs, device_tokens, groups, pt, prompts):
+@pytest.mark.parametrize("bs,device_tokens,groups,pt,prompts,dtype,D", [
+    (16, False, False, 32, (20, 70), W.F16, 64), (8, False, False, 32, (20, 70), W.F16, 64),
+    (16, True, False, 32, (20, 70), W.F16, 64), (16, True, True, 32, (20, 70), W.F16, 64),
+    (8, False, True, 32, (20, 70), W.F16, 64), (16, True, True, 0, (100, 300), W.F16, 64),
+    (32, True, False, 0, (100, 300), W.BF16, 128), (32, True, True, 0, (100, 300), W.BF16, 128),
+    (64, False, True, 64, (130, 400), W.F16, 128)])
+def test_beam_search_steps_match_oracle(bs, device_tokens, groups, pt, prompts, dtype, D):
     """groups: the beams of each request decode as a prefix group over
     their prompt's full blocks, which stay shared for the whole search."""
     bw = W.beam_search(seed=7 + bs, requests=3, beams=4, prompt_lo=prompts[0],
-                       prompt_hi=prompts[1], steps=6, H=4, D=64, bs=bs)
+                       prompt_hi=prompts[1], steps=6, H=4, D=D, bs=bs, dtype=dtype)
     st = device_step(bw.init, pt)
     st.plan()
     if groups:
