@@ -16,7 +16,7 @@ import torch
 import workloads as W
 from oracle import kernels as K
 from oracle import step as OS
-from oracle.allocator import BlockAllocatorModel, OutOfBlocks
+from oracle.allocator import BlockAllocatorModel, OutOfBlocks, fork_tables
 from tests.trace_replay import GOLDEN, check_expect, load_traces, replay
 
 
@@ -441,3 +441,145 @@ def test_swap_blocks_round_trip_and_fancy_indexing():
         assert np.array_equal(g2k[g1], gk[g0]) and np.array_equal(g2v[g1], gv[g0])
     untouched = [b for b in range(NBg) if b not in (1, 4, 9)]
     assert np.array_equal(g2k[untouched], gk[untouched])
+
+
+# ------------------------------------------------------------ beam search
+# Values worked out by hand from the pages' rules (share = one more hold per
+# block, a block returns to the free list when its count reaches 0, copy on
+# write into a block held by more than one table) and the oracle's readings
+# (a stack free list: a fresh pool of 12 hands out 11, 10, 9, ...; a fork
+# takes the new holds first, then releases the old tables row by row, slot
+# by slot).  Sources: "3.3 页面级显存管理" 3.3.2 (share_blocks); notes on
+# "vLLM: Easy, Fast, and Cheap LLM Serving with PagedAttention", section
+# "Memory Sharing与写时复制" (beams share blocks until they diverge).
+def _fork_fixture():
+    a = BlockAllocatorModel(12)
+    t0 = a.alloc(3)                                  # request 0, beam 0
+    a.incref([t0[0]])
+    t1 = [t0[0]] + a.alloc(2)                        # request 0, beam 1
+    t2 = a.alloc(2)                                  # request 1, beam 0
+    a.incref([t2[0]])
+    t3 = [t2[0]] + a.alloc(1)                        # request 1, beam 1
+    assert [t0, t1, t2, t3] == [[11, 10, 9], [11, 8, 7], [6, 5], [6, 4]]
+    assert a.rc == {11: 2, 10: 1, 9: 1, 8: 1, 7: 1, 6: 2, 5: 1, 4: 1}
+    return a, [t0, t1, t2, t3]
+
+
+FORK_PINS = [
+    # parents, tables after, refcounts after, free list after (top last),
+    # the ids the next allocation hands out
+    ([1, 1, 3, 2],
+     [[11, 8, 7], [11, 8, 7], [6, 4], [6, 5]],
+     {11: 2, 8: 2, 7: 2, 6: 2, 5: 1, 4: 1},
+     [0, 1, 2, 3, 10, 9], [9, 10, 3]),
+    # two rows lose every child: row 0 frees 10 then 9, row 2 frees 5
+    ([1, 1, 3, 3],
+     [[11, 8, 7], [11, 8, 7], [6, 4], [6, 4]],
+     {11: 2, 8: 2, 7: 2, 6: 2, 4: 2},
+     [0, 1, 2, 3, 10, 9, 5], [5, 9, 10, 3]),
+]
+
+
+def _fork_pin_holds(fork):
+    for parents, tables, rc, free, nxt in FORK_PINS:
+        a, old = _fork_fixture()
+        new = fork(a, old, parents)
+        if not (new == tables and a.rc == rc and a.free == free and a.alloc(len(nxt)) == nxt):
+            return False
+    return True
+
+
+def test_fork_tables_hand_worked():
+    assert _fork_pin_holds(fork_tables)
+
+
+def test_fork_pin_catches_release_in_reverse_row_order():
+    """A planted mistake (old tables released last row first) changes which
+    blocks the next allocation receives, and the pin sees it."""
+    def reversed_rows(alloc, tables, parents):
+        new = [list(tables[int(p)]) for p in parents]
+        for t in new:
+            alloc.incref(t)
+        for t in reversed(tables):
+            alloc.decref(t)
+        return new
+    assert not _fork_pin_holds(reversed_rows)
+
+
+def _beam_fixture():
+    """2 requests x 2 beams, 1 head, D = 8, fp16, blocks of 4 tokens, pool of
+    10.  Request 0's prompt is 6 tokens in blocks [7, 3]; request 1's is 4
+    tokens in block [5]; both beams of a request hold the prompt's blocks.
+    Every V row is one constant (prompt token p of request 0: p; of request
+    1: 10 + p; new tokens: 16, 20, 24, 28 at step 1 and 32, 40, 48, 56 at
+    step 2, by beam) and q = 0, so each output is the plain mean of the V
+    values on the sequence's path."""
+    f16 = W.F16
+    S, H, D, bs, NB, MB = 4, 1, 8, 4, 10, 3
+    poison = W.POISON[f16]
+    blocks = np.array([3, 5, 7], dtype=np.int32)
+
+    def rows(vals):                                  # one block of V (or K)
+        out = np.full((bs, H, D), poison, dtype=np.uint16)
+        for off, v in enumerate(vals):
+            out[off] = W.to_bits(np.full((H, D), v, np.float32), f16)
+        return out
+    v_blocks = np.stack([rows([4, 5]), rows([10, 11, 12, 13]), rows([0, 1, 2, 3])])
+    k_blocks = np.stack([rows([1, 1]), rows([1, 1, 1, 1]), rows([1, 1, 1, 1])])
+    tables = np.array([[7, 3, -1], [7, 3, -1], [5, -1, -1], [5, -1, -1]], dtype=np.int32)
+    empty = np.zeros((0, H, D), dtype=np.uint16)
+    init = W.Workload(name="beam_pin", dtype=f16, S=S, H=H, D=D, bs=bs, NB=NB, MB=MB,
+                      scale=1.0 / math.sqrt(D), ctx_before=np.array([6, 6, 4, 4], np.int32),
+                      n_new=np.zeros(S, np.int32), tables_pre=tables,
+                      nblocks_pre=np.array([2, 2, 1, 1], np.int32),
+                      initial_free=np.array([0, 1, 2, 4, 6, 8, 9], np.int32),
+                      blocks=blocks, k_blocks=k_blocks, v_blocks=v_blocks,
+                      q=np.zeros((S, H, D), np.uint16), new_k=empty, new_v=empty,
+                      seq_idx=np.zeros(0, np.int32), pos=np.zeros(0, np.int32))
+    new_v = np.stack([W.to_bits(np.repeat(np.array(v, np.float32)[:, None, None], D, 2), f16)
+                      for v in ([16, 20, 24, 28], [32, 40, 48, 56])])
+    new_k = W.to_bits(np.ones((2, S, H, D), np.float32), f16)
+    return W.BeamWorkload(init=init, beams=2,
+                          parents=np.array([[1, 0, 3, 3], [0, 0, 2, 3]], np.int32),
+                          new_k=new_k, new_v=new_v, q=np.zeros((2, S, H, D), np.uint16))
+
+
+# Step 1: the fork changes no count.  Beam 0 writes position 6 into block 3,
+# held twice, so it copies 3 to the top of the free list (9); beam 1 then
+# holds 3 alone and writes in place; beams 2 and 3 open blocks 8 and 6.
+# Step 2: old beam 1 has no child, so its block 3 drops to 0 and goes back
+# on top of the free list; beam 0's write into the shared block 9 copies it
+# into that same block 3.
+BEAM_PINS = [
+    ([[7, 9, -1], [7, 3, -1], [5, 8, -1], [5, 6, -1]], [[3, 9]],
+     [9 * 4 + 2, 3 * 4 + 2, 8 * 4 + 0, 6 * 4 + 0],
+     [(15 + 16) / 7, (15 + 20) / 7, (46 + 24) / 5, (46 + 28) / 5]),
+    ([[7, 3, -1], [7, 9, -1], [5, 8, -1], [5, 6, -1]], [[9, 3]],
+     [3 * 4 + 3, 9 * 4 + 3, 8 * 4 + 1, 6 * 4 + 1],
+     [(15 + 16 + 32) / 8, (15 + 16 + 40) / 8, (46 + 24 + 48) / 6, (46 + 28 + 56) / 6]),
+]
+
+
+def _beam_pin_holds():
+    steps = list(OS.run_beam(_beam_fixture(), nthreads=1))
+    if len(steps) != len(BEAM_PINS):
+        return False
+    for (bt, pairs, slots, _k, _v, _ids, out), (t, p, sl, mean) in zip(steps, BEAM_PINS):
+        want = np.broadcast_to(np.array(mean)[:, None, None], out.shape)
+        if not (np.array_equal(bt, t) and np.array_equal(pairs, np.array(p).reshape(-1, 2))
+                and np.array_equal(slots, sl) and np.allclose(out, want, rtol=0, atol=1e-12)):
+            return False
+    return True
+
+
+def test_run_beam_hand_worked():
+    assert _beam_pin_holds()
+
+
+def test_beam_pin_catches_slot_one_past_the_context(monkeypatch):
+    """A planted mistake (the new token mapped at position ctx + 1 instead of
+    ctx) moves the write and the slots, and the pin sees it."""
+    real = OS.kernels.slot_mapping
+    monkeypatch.setattr(OS.kernels, "slot_mapping",
+                        lambda bt, seq, pos, bs: real(bt, seq, np.asarray(pos) + 1, bs))
+    assert not _beam_pin_holds()
