@@ -60,7 +60,8 @@ typedef enum {
     PKV_ERR_UNSUPPORTED = 2, /* head_dim / block_size / dtype not built   */
     PKV_ERR_OOM = 3,         /* allocator: not enough free blocks          */
     PKV_ERR_WORKSPACE = 4,   /* decode: workspace too small               */
-    PKV_ERR_CUDA = 5         /* a CUDA runtime call failed                */
+    PKV_ERR_CUDA = 5,        /* a CUDA runtime call failed                */
+    PKV_ERR_HOST_MEMORY = 6  /* the library's own host allocation failed  */
 } pkv_status;
 
 typedef enum { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype;
@@ -261,6 +262,15 @@ pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_ma
                            int P, int H, int D, int bs, int NB, pkv_dtype dtype,
                            void* stream);
 
+/* Host-side check of pkv_copy_blocks' precondition on a copy list the
+ * caller holds in host memory (pairs [P][2] int64, (src, dst)): every id in
+ * [0, NB), no dst twice, no dst that is also a src.  PKV_OK if it holds,
+ * PKV_ERR_INVALID_ARG (naming the first offending pair) if not,
+ * PKV_ERR_HOST_MEMORY if the check's scratch cannot be allocated.  Reads
+ * only; O(P log P).  pkv_beam_step runs it on its own pairs before the
+ * upload. */
+pkv_status pkv_check_copy_pairs(const int64_t* pairs, int32_t P, int32_t NB);
+
 /* Swap directions for pkv_swap_blocks. */
 #define PKV_SWAP_OUT 0 /* GPU cache -> host cache */
 #define PKV_SWAP_IN 1  /* host cache -> GPU cache */
@@ -404,7 +414,7 @@ int32_t pkv_alloc_num_shared(const pkv_allocator* a);
  *   2. pkv_alloc_append_batch for one new token per sequence, after
  *      ctx_before[s] = context_lens[parents[s]] (the old lengths): the
  *      copy-on-write pairs of shared last blocks, new blocks at block
- *      boundaries;
+ *      boundaries; the pairs then pass pkv_check_copy_pairs;
  *   3. context_lens[s] = ctx_before[s] + 1 (host array, in place);
  *   4. the tables, lengths, token positions (ctx_before), sequence index
  *      (0..S-1) and copy pairs are written into `staging` and uploaded to
@@ -440,8 +450,9 @@ int32_t pkv_alloc_num_shared(const pkv_allocator* a);
  * Errors: arguments are checked before step 1 (PKV_ERR_INVALID_ARG: a
  * parent out of range, a context that would pass the table, buffers too
  * small or misaligned).  A failure of step 1 changes nothing; a failure of
- * step 2 (PKV_ERR_OOM) leaves the fork done and the first sequences
- * extended, as pkv_alloc_append_batch describes, and launches nothing.  A
+ * step 2 (PKV_ERR_OOM, or pairs that fail pkv_check_copy_pairs) leaves the
+ * fork done and the first sequences extended, as pkv_alloc_append_batch
+ * describes, and launches nothing.  A
  * failure in steps 4-5 (PKV_ERR_CUDA, or an argument pkv_copy_blocks or
  * pkv_decode_step rejects) comes after steps 1-3 have updated the host
  * arrays and the allocator. */

@@ -21,6 +21,7 @@ PKV_ERR_UNSUPPORTED = 2
 PKV_ERR_OOM = 3
 PKV_ERR_WORKSPACE = 4
 PKV_ERR_CUDA = 5
+PKV_ERR_HOST_MEMORY = 6
 PKV_F16 = 0
 PKV_BF16 = 1
 PKV_DEVERR_BLOCK_ID = 0x1
@@ -34,7 +35,8 @@ PKV_SWAP_OUT = 0
 PKV_SWAP_IN = 1
 
 _STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
-                 3: "PKV_ERR_OOM", 4: "PKV_ERR_WORKSPACE", 5: "PKV_ERR_CUDA"}
+                 3: "PKV_ERR_OOM", 4: "PKV_ERR_WORKSPACE", 5: "PKV_ERR_CUDA",
+                 6: "PKV_ERR_HOST_MEMORY"}
 
 
 class PkvError(RuntimeError):
@@ -70,6 +72,7 @@ SIGNATURES = {
     "pkv_compute_slot_mapping": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "pkv_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "pkv_copy_blocks": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "pkv_check_copy_pairs": (_I, [_P, _I32, _I32]),
     "pkv_swap_blocks": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P]),
     "pkv_sync_check": (_I, [_P]),
     "pkv_get_device_errors": (_I, [_P]),

@@ -148,12 +148,23 @@ def plan_step(alloc: BlockAllocator, tables_pre: np.ndarray, nblocks_pre: np.nda
     """Host part of one decode step: for every sequence in order, make room
     for its new tokens (copy-on-write of shared blocks, then new blocks).
 
-    Returns (tables [S, MB] int32, nblocks [S] int32, pairs [P, 2] int64).
+    Returns (tables [S, MB] int32, nblocks [S] int32, pairs [P, 2] int64);
+    the pairs have passed pkv_check_copy_pairs (pkv_copy_blocks'
+    precondition) before they are returned.
     """
     tables = np.array(tables_pre, dtype=np.int32, copy=True, order="C")
     nb = np.array(nblocks_pre, dtype=np.int32, copy=True)
     pairs = alloc.append_batch(tables, nb, ctx_before, n_new, block_size)
+    check_copy_pairs(pairs, alloc.num_blocks)
     return tables, nb, pairs
+
+
+def check_copy_pairs(pairs: np.ndarray, num_blocks: int) -> None:
+    """Raises PkvError unless the (src, dst) copy list meets pkv_copy_blocks'
+    precondition: ids in [0, num_blocks), no dst twice, no dst also a src."""
+    p = np.ascontiguousarray(pairs, dtype=np.int64).reshape(-1, 2)
+    check(lib().pkv_check_copy_pairs(p.ctypes.data if len(p) else None, len(p), int(num_blocks)),
+          "check_copy_pairs")
 
 
 def plan_swap_out(gpu: BlockAllocator, host: BlockAllocator, table):
@@ -173,19 +184,3 @@ def plan_swap_in(gpu: BlockAllocator, host: BlockAllocator, host_ids):
     pairs = np.array(list(zip(host_ids, table)), dtype=np.int64).reshape(-1, 2)
     return table, pairs
 
-
-def fork_tables(alloc: BlockAllocator, tables: list, parents) -> list:
-    """Beam-search / parallel-sampling fork: sequence b continues from
-    sequence parents[b].  Each new table takes a hold on every block of its
-    parent's table (sharing, "3.3 页面级显存管理" 3.3.2), then the old tables
-    are released, so blocks that survive the fork never reach refcount 0.
-    The next write into a block shared this way is copied first
-    (copy-on-write, by `append`)."""
-    new = [list(tables[int(p)]) for p in parents]
-    ids = [b for t in new for b in t]
-    if ids:
-        alloc.incref(ids)
-    old = [b for t in tables for b in t]
-    if old:
-        alloc.decref(old)
-    return new

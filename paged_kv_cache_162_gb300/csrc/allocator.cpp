@@ -14,8 +14,10 @@
 // inputs before changing anything, so a failure leaves the pool as it was.
 #include <algorithm>
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <new>
+#include <utility>
 #include <vector>
 
 #include "pagedkv.h"
@@ -60,7 +62,7 @@ pkv_status pkv_alloc_create(int32_t num_blocks, pkv_allocator** out) {
     pkv::clear_error();
     if (!out || num_blocks < 0) return pkv::fail(PKV_ERR_INVALID_ARG, "alloc_create: bad argument");
     pkv_allocator* a = new (std::nothrow) pkv_allocator();
-    if (!a) return pkv::fail(PKV_ERR_INVALID_ARG, "alloc_create: out of host memory");
+    if (!a) return pkv::fail(PKV_ERR_HOST_MEMORY, "alloc_create: out of host memory");
     try {
         a->num_blocks = num_blocks;
         a->stack.resize(num_blocks);
@@ -68,7 +70,7 @@ pkv_status pkv_alloc_create(int32_t num_blocks, pkv_allocator** out) {
         a->delta.assign(num_blocks, 0);
     } catch (...) {
         delete a;
-        return pkv::fail(PKV_ERR_INVALID_ARG, "alloc_create: out of host memory");
+        return pkv::fail(PKV_ERR_HOST_MEMORY, "alloc_create: out of host memory");
     }
     // popping from the top hands out num_blocks-1 first
     for (int32_t i = 0; i < num_blocks; ++i) a->stack[i] = i;
@@ -82,7 +84,12 @@ pkv_status pkv_alloc_create_with_order(int32_t num_blocks, const int32_t* initia
     pkv::clear_error();
     if (!out || num_blocks < 0 || n_free < 0 || n_free > num_blocks || (n_free && !initial_free))
         return pkv::fail(PKV_ERR_INVALID_ARG, "alloc_create_with_order: bad argument");
-    std::vector<uint8_t> seen(num_blocks, 0);
+    std::vector<uint8_t> seen;
+    try {
+        seen.assign(num_blocks, 0);
+    } catch (...) {
+        return pkv::fail(PKV_ERR_HOST_MEMORY, "alloc_create_with_order: out of host memory");
+    }
     for (int32_t i = 0; i < n_free; ++i) {
         int32_t id = initial_free[i];
         if (id < 0 || id >= num_blocks || seen[id])
@@ -222,7 +229,11 @@ pkv_status pkv_alloc_append_batch(pkv_allocator* a, int32_t* tables, int32_t* nu
         std::vector<int64_t> big;
         int64_t* buf = one;
         if (cap > 64) {
-            big.resize(2 * cap);
+            try {
+                big.resize(2 * cap);
+            } catch (...) {
+                return pkv::fail(PKV_ERR_HOST_MEMORY, "alloc_append_batch: out of host memory");
+            }
             buf = big.data();
         }
         // refuse before touching sequence s if its copies might not fit
@@ -269,7 +280,7 @@ pkv_status pkv_alloc_fork(pkv_allocator* a, int32_t* tables, int32_t* num_blocks
         a->nchild.assign(S, 0);
         a->rows.assign(tables, tables + (size_t)S * MB);
     } catch (...) {
-        return pkv::fail(PKV_ERR_INVALID_ARG, "alloc_fork: out of host memory");
+        return pkv::fail(PKV_ERR_HOST_MEMORY, "alloc_fork: out of host memory");
     }
     int32_t* nchild = a->nchild.data();
     const int32_t* old_tab = a->rows.data();
@@ -318,6 +329,45 @@ pkv_status pkv_alloc_refcount(const pkv_allocator* a, int32_t id, int32_t* rc) {
     pkv::clear_error();
     if (!a || !rc || !valid_id(a, id)) return pkv::fail(PKV_ERR_INVALID_ARG, "alloc_refcount: bad argument");
     *rc = a->rc[id];
+    return PKV_OK;
+}
+
+pkv_status pkv_check_copy_pairs(const int64_t* pairs, int32_t P, int32_t NB) {
+    pkv::clear_error();
+    if (P < 0 || NB < 0 || (P > 0 && !pairs)) return pkv::fail(PKV_ERR_INVALID_ARG, "check_copy_pairs: bad argument");
+    char msg[160];
+    for (int32_t i = 0; i < P; ++i) {
+        if (pairs[2 * i] < 0 || pairs[2 * i] >= NB || pairs[2 * i + 1] < 0 || pairs[2 * i + 1] >= NB) {
+            snprintf(msg, sizeof msg, "check_copy_pairs: pair %d holds an id outside [0, %d)", i, NB);
+            return pkv::fail(PKV_ERR_INVALID_ARG, msg);
+        }
+    }
+    // (dst, pair index) sorted by dst: a repeated dst sits next to its twin,
+    // and each src is looked up among the dsts by binary search
+    std::vector<std::pair<int64_t, int32_t>> dst;
+    try {
+        dst.resize(P);
+    } catch (...) {
+        return pkv::fail(PKV_ERR_HOST_MEMORY, "check_copy_pairs: out of host memory");
+    }
+    for (int32_t i = 0; i < P; ++i) dst[i] = {pairs[2 * i + 1], i};
+    std::sort(dst.begin(), dst.end());
+    for (int32_t i = 1; i < P; ++i) {
+        if (dst[i].first == dst[i - 1].first) {
+            snprintf(msg, sizeof msg, "check_copy_pairs: pairs %d and %d copy into the same block %lld",
+                     dst[i - 1].second, dst[i].second, (long long)dst[i].first);
+            return pkv::fail(PKV_ERR_INVALID_ARG, msg);
+        }
+    }
+    for (int32_t i = 0; i < P; ++i) {
+        const int64_t src = pairs[2 * i];
+        auto it = std::lower_bound(dst.begin(), dst.end(), std::make_pair(src, (int32_t)-1));
+        if (it != dst.end() && it->first == src) {
+            snprintf(msg, sizeof msg, "check_copy_pairs: block %lld is the source of pair %d and the target of pair %d",
+                     (long long)src, i, it->second);
+            return pkv::fail(PKV_ERR_INVALID_ARG, msg);
+        }
+    }
     return PKV_OK;
 }
 

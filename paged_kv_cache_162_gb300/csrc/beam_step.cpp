@@ -97,6 +97,10 @@ pkv_status pkv_beam_step(pkv_allocator* a, int32_t* tables, int32_t* num_blocks,
     st = pkv_alloc_append_batch(a, tables, num_blocks, S, MB, pos, seq, bs, pairs, 2 * S, &np,
                                 &ndone);
     if (st != PKV_OK) return st;  // forked; rows [0, ndone) extended, nothing launched
+    // the copies must meet pkv_copy_blocks' precondition before any of them
+    // reaches the device
+    st = pkv_check_copy_pairs(pairs, np, NB);
+    if (st != PKV_OK) return st;
     for (int32_t s = 0; s < S; ++s) {
         context_lens[s] = pos[s] + 1;
         ctx[s] = context_lens[s];

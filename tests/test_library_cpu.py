@@ -56,7 +56,7 @@ def test_binding_constants_equal_the_header():
     included, so a bit read back from the device decodes the same way."""
     consts = header_constants()
     for name in ["PKV_OK", "PKV_ERR_INVALID_ARG", "PKV_ERR_UNSUPPORTED", "PKV_ERR_OOM",
-                 "PKV_ERR_WORKSPACE", "PKV_ERR_CUDA", "PKV_F16", "PKV_BF16",
+                 "PKV_ERR_WORKSPACE", "PKV_ERR_CUDA", "PKV_ERR_HOST_MEMORY", "PKV_F16", "PKV_BF16",
                  "PKV_DEVERR_BLOCK_ID", "PKV_DEVERR_SLOT", "PKV_DEVERR_CONTEXT",
                  "PKV_DEVERR_POSITION", "PKV_DEVERR_GROUP", "PKV_DEVERR_TIMEOUT",
                  "PKV_NOALLOC_SCRATCH_BYTES", "PKV_SWAP_OUT", "PKV_SWAP_IN"]:
@@ -431,3 +431,31 @@ def test_in_place_arrays_must_be_int32_contiguous():
     with pytest.raises(L.PkvError):
         a.append_row(np.full(8, -1, dtype=np.int32)[::2], 0, 0, 1, 16)
     assert a.num_free == 16
+
+
+def test_check_copy_pairs_accepts_allocator_copies_and_names_the_bad_pair():
+    """pkv_copy_blocks' precondition, checked on the host: ids in the pool,
+    no destination twice, no destination that is also a source."""
+    from paged_kv_cache_162_gb300.allocator import check_copy_pairs
+    a = BlockAllocator(40)
+    t = np.full((8, 4), -1, np.int32)
+    nb = np.zeros(8, np.int32)
+    a.append_batch(t, nb, np.zeros(8, np.int32), np.full(8, 20, np.int32), 16)
+    forked = t.copy()
+    fnb = nb.copy()
+    a.fork(forked, fnb, np.array([0, 0, 1, 1, 2, 2, 3, 3], np.int32))
+    pairs = a.append_batch(forked, fnb, np.full(8, 20, np.int32), np.ones(8, np.int32), 16)
+    assert len(pairs) == 4            # first beam of each shared row copies
+    check_copy_pairs(pairs, 40)
+    check_copy_pairs(np.zeros((0, 2), np.int64), 40)
+    cases = {
+        "outside": [[1, 2], [3, 40]],
+        "same block": [[1, 2], [3, 2]],
+        "source of pair 1": [[1, 2], [2, 5]],
+        "source of pair 0": [[4, 4]],
+    }
+    for what, p in cases.items():
+        with pytest.raises(L.PkvError) as e:
+            check_copy_pairs(np.array(p, np.int64), 40)
+        assert e.value.status == L.PKV_ERR_INVALID_ARG and what in str(e.value), (what, e.value)
+    assert L.lib().pkv_check_copy_pairs(None, -1, 40) == L.PKV_ERR_INVALID_ARG
