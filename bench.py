@@ -548,7 +548,15 @@ def run_ours(args):
                          "peak_source": peak_kind,
                          "kernel": "pkv paged_attention_decode (plan + decode kernels), events "
                                    "around each call in a second run of the step loop",
-                         "algorithmic_bytes_per_launch": dec_bytes},
+                         "algorithmic_bytes_per_launch": dec_bytes,
+                         "frac_of_step": dec_bytes / (step_ms * 1e-3) / 1e9 / peak,
+                         "clocks_note": "frac uses decode_ms, the decode call alone with an "
+                                        "event pair around it; the pair costs the call its "
+                                        "launch overlap with the kernel before it, so decode_ms "
+                                        "can exceed ms_per_step, which also holds the prologue "
+                                        "kernel.  frac_of_step divides the same bytes by the "
+                                        "whole timed step (region A's clock): a lower bound "
+                                        "on the decode kernel's fraction"},
             "cpu_baseline": cpu,
             "e2e": {"value": weak_value(kv_bytes, world, e2e_ms), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,

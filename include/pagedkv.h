@@ -202,23 +202,34 @@ pkv_status pkv_paged_attention_decode_shared_prefix(
  * that owns every byte of device memory and hands it out only through its
  * own pool, a latency-critical loop where a cudaMalloc could synchronise
  * the whole device, or a small C host program with no device allocator of
- * its own.  This entry point computes exactly what
- * pkv_paged_attention_decode computes, with the same arguments except the
- * workspace, and allocates nothing (no cudaMalloc, no cudaFree).
+ * its own.  This entry point takes the same arguments as
+ * pkv_paged_attention_decode except the workspace, runs the same kernels,
+ * and allocates nothing (no cudaMalloc, no cudaFree).
  *
  * Its split-K scratch is a static device array of PKV_NOALLOC_SCRATCH_BYTES
  * inside the library: every GPU that loads the library holds one copy until
- * the process exits.  A call whose scratch need (pkv_decode_workspace_size
- * of the same S, H, D, max_context_len, partition_tokens) exceeds it
- * returns PKV_ERR_WORKSPACE; use pkv_paged_attention_decode with a caller
- * workspace for such sizes.
+ * the process exits.
+ *   - A fixed partition_tokens > 0 gives pkv_paged_attention_decode's
+ *     result at that partition size bit for bit; a call whose need
+ *     (pkv_decode_workspace_size of the same S, H, D, max_context_len,
+ *     partition_tokens) exceeds the array returns PKV_ERR_WORKSPACE.
+ *   - partition_tokens = 0 starts the automatic choice from the smallest of
+ *     64, 128, ..., 4096 tokens whose partials fit the array, so it may run
+ *     larger partitions than pkv_paged_attention_decode would: the result
+ *     then agrees with it within the attention tolerance, not bit for bit.
+ *     Only a size that does not fit even at 4096-token partitions returns
+ *     PKV_ERR_WORKSPACE.
+ * Use pkv_paged_attention_decode with a caller workspace for larger sizes.
  *
- * The first call on a device looks up the array's device address with that
- * device current; make that first call before any stream capture begins.
- * All calls on a device share the one array, which keeps the last call's
- * contents; each call resets what it reads before reading it.  Calls that
- * overlap on the GPU (other streams, other host threads) race on the array
- * and give wrong results: serialise them. */
+ * The first call in a device's context looks up the array's device address
+ * with that device current; make that first call before any stream capture
+ * begins.  The address is kept per device together with the id of the
+ * context it was found in: after a device reset the next call sees a new
+ * context and looks the address up again (so that call, too, should come
+ * before any capture).  All calls on a device share the one array, which
+ * keeps the last call's contents; each call resets what it reads before
+ * reading it.  Calls that overlap on the GPU (other streams, other host
+ * threads) race on the array and give wrong results: serialise them. */
 pkv_status pkv_paged_attention_decode_noalloc(
     void* out, const void* q, const void* k_cache, const void* v_cache,
     const int32_t* block_tables, const int32_t* context_lens,

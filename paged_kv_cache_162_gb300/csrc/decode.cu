@@ -27,6 +27,12 @@
 //    the V loads of tile t are in flight while q.K(t) is computed, the K
 //    loads of tile t+1 while P.V(t) is accumulated.  Full tiles take no
 //    per-row predicates.
+//  * Block table: each warp keeps a window of 64 of its partition's table
+//    entries in shared memory, filled by one coalesced load across its lanes
+//    and refilled when a tile passes the window, so a tile's lookup is a
+//    shared-memory read ("3.1 PagedAttention的核心原理" 3.1.3: the kernel
+//    indexes a flat block_table array).  Tile t+1's lookup is made while
+//    tile t is computed, so it stays off the load chain.
 //  * Partitions: a context longer than PT tokens is split.  Each partition
 //    writes (running max, running sum, unnormalised output) to the
 //    workspace; the CTA that finishes a (sequence, head group) last -- known
@@ -535,9 +541,14 @@ __device__ __forceinline__ void load_tile(uint4 (&dst)[NI], const uint16_t* cons
     }
 }
 
+constexpr int kWarpWindow = 64;  // table entries one warp holds in shared memory
+
+// `wtab` is this warp's window of kWarpWindow table entries in shared
+// memory, refilled (by the whole warp) when a tile's block falls outside it.
 template <class E, int D, int BS>
 __device__ __forceinline__ void attend_partition(const DecodeParams& a, int s, int h, int part,
-                                                 int t_begin, int t_end, int np, int lane) {
+                                                 int t_begin, int t_end, int np, int lane,
+                                                 int* wtab) {
     constexpr int LPR = D / 8;         // lanes per row: 16 bytes each
     constexpr int RPI = 32 / LPR;      // rows per warp-wide load
     constexpr int NI = kTile / RPI;    // warp-wide loads per tile (K and V each)
@@ -556,6 +567,22 @@ __device__ __forceinline__ void attend_partition(const DecodeParams& a, int s, i
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j] = 0.f;
 
+    // the window covers logical blocks [win0, win0 + kWarpWindow); entries
+    // past the partition's last block are not read
+    const int lb_last = t_end > t_begin ? (t_end - 1) / BS : 0;
+    int win0 = -kWarpWindow;
+    auto entry = [&](int lb) -> int {
+        if ((unsigned)(lb - win0) >= (unsigned)kWarpWindow) {  // the same in every lane
+            __syncwarp();
+            win0 = lb;
+#pragma unroll
+            for (int i = lane; i < kWarpWindow; i += 32)
+                if (lb + i <= lb_last) wtab[i] = __ldg(bt_row + lb + i);
+            __syncwarp();
+        }
+        return wtab[lb - win0];
+    };
+
     constexpr int TB = (BS < kTile) ? kTile / BS : 1;  // blocks per tile
     // element offsets of the tile at t0 in each of its TB blocks, and its
     // valid rows (masked from the first block whose id is out of range)
@@ -567,7 +594,7 @@ __device__ __forceinline__ void attend_partition(const DecodeParams& a, int s, i
             int phys = 0;
             if (tb < t_end) {
                 const int lb = tb / BS;
-                phys = __ldg(bt_row + lb);
+                phys = entry(lb);
                 if ((unsigned)phys >= (unsigned)a.NB) {
                     if (lane == 0) pkv::report(a.err, PKV_DEVERR_BLOCK_ID);
                     nvalid = min(nvalid, b * BS);
@@ -778,6 +805,7 @@ __global__ void __launch_bounds__(kThreads, PKV_MIN_CTAS_PER_SM) decode_kernel(D
     asm volatile("griddepcontrol.wait;" ::: "memory");
     __shared__ int s_item;
     __shared__ int s_last;
+    __shared__ int s_tab[kWarps][kWarpWindow];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int total = *a.ws.n_items * a.HG;
     const int PT = *a.ws.pt;
@@ -795,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, PKV_MIN_CTAS_PER_SM) decode_kernel(D
         const int t_begin = part * PT;
         const int t_end = min(t_begin + PT, ctx);
         const int h = hg * kWarps + warp;
-        if (h < a.H) attend_partition<E, D, BS>(a, s, h, part, t_begin, t_end, np, lane);
+        if (h < a.H) attend_partition<E, D, BS>(a, s, h, part, t_begin, t_end, np, lane, s_tab[warp]);
         if (np > 1) {
             __threadfence();
             __syncthreads();
@@ -1619,9 +1647,39 @@ namespace {
 constexpr int kNoAllocMaxDevices = 64;
 std::mutex g_noalloc_mu;
 void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+unsigned long long g_noalloc_ctx[kNoAllocMaxDevices] = {};
 
-// Device address of the scratch array on the current device, looked up once
-// per device with that device current.
+// Unique id of the calling thread's current context; 0 when there is none
+// or the driver does not offer the lookup.  A device reset ends the
+// context, and the array lives at a new address in the next one.
+unsigned long long current_context_id() {
+    using GetCurrent = CUresult (*)(CUcontext*);
+    using GetId = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(f);
+        cudaGetLastError();
+    });
+    CUcontext c = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&c) != CUDA_SUCCESS || !c ||
+        get_id(c, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of the scratch array on the current device, looked up with
+// that device current once per context of the device.
 pkv_status noalloc_scratch(void** addr) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1629,7 +1687,8 @@ pkv_status noalloc_scratch(void** addr) {
     if (dev < 0 || dev >= kNoAllocMaxDevices)
         return pkv::fail(PKV_ERR_INVALID_ARG, "paged_attention_decode_noalloc: device ordinal above 63");
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (!g_noalloc_addr[dev]) {
+    const unsigned long long ctx = current_context_id();
+    if (!g_noalloc_addr[dev] || ctx == 0 || ctx != g_noalloc_ctx[dev]) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || !p) {
@@ -1637,6 +1696,8 @@ pkv_status noalloc_scratch(void** addr) {
             return pkv::cuda_fail(e, "paged_attention_decode_noalloc: cudaGetSymbolAddress of the scratch array");
         }
         g_noalloc_addr[dev] = p;
+        // the lookup made the context current if it was not yet
+        g_noalloc_ctx[dev] = current_context_id();
     }
     *addr = g_noalloc_addr[dev];
     return PKV_OK;
