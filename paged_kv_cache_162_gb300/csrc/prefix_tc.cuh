@@ -34,13 +34,18 @@ constexpr int kTcD = 128;                       // head_dim of this path
 constexpr int kTcTile = 128;                    // tokens per K or V tile
 constexpr int kTcCtasPerSm = 2;                 // CTAs resident per SM
 constexpr int kTcStages = 3;                    // tiles in flight per CTA
-constexpr int kTcChunkTiles = 2;                // tiles per softmax chunk
+constexpr int kTcChunkTiles = 1;                // tiles per softmax chunk
 constexpr int kTcHalf = kTcTile * 128;          // bytes of one 64-dim half of a tile (16 KB)
 constexpr int kTcTileBytes = 2 * kTcHalf;       // 32 KB
 constexpr int kTcQOff = kTcStages * kTcTileBytes;       // Q: 16 rows x 256 B (2 halves of 2 KB)
-constexpr int kTcPOff = kTcQOff + 4096;                 // P: chunk tiles x 4 KB
-constexpr int kTcBarOff = kTcPOff + kTcChunkTiles * 4096;
-constexpr int kTcSmemBytes = kTcBarOff + 1024 + 1024;   // barriers, TMEM slot, reductions; +1 KB alignment
+constexpr int kTcPBytes = kTcChunkTiles * 4096;         // P of one chunk
+constexpr int kTcPOff = kTcQOff + 4096;                 // P: two chunk buffers, used in turn
+constexpr int kTcBarOff = kTcPOff + 2 * kTcPBytes;
+constexpr int kTcSmemBytes = kTcBarOff + 2048 + 1024;   // barriers, TMEM slot, reductions; +1 KB alignment
+// The softmax keeps a per-member reference max and moves it only when a
+// chunk's max passes it by more than this (log2 units): P stays below 2^8,
+// and O in TMEM is rescaled (waiting for the previous P.V) only then.
+constexpr float kTcLazy = 8.f;
 constexpr int kTcSCols = 16 * kTcChunkTiles;    // TMEM columns of one S buffer
 constexpr int kTcOCol = 2 * kTcSCols;           // O after the two S buffers
 constexpr int kTcTmemCols = kTcOCol + 16 <= 32 ? 32 : kTcOCol + 16 <= 64 ? 64
@@ -49,6 +54,7 @@ constexpr int kTcThreads = 192;                 // warps 0-3 softmax, 4 loads, 5
 
 static_assert(kTcCtasPerSm * (kTcSmemBytes + 1024) <= 228 * 1024, "prefix_tc shared memory");
 static_assert(16 * kTcStages + 72 + 4 <= 256, "prefix_tc barriers overlap the reductions");
+static_assert(kTcChunkTiles == 1, "the softmax below handles one tile per chunk");
 static_assert(kTcCtasPerSm * kTcTmemCols <= 512, "prefix_tc TMEM");
 
 // ---- PTX helpers (the mbarrier waits and TMEM fences are in tc_wait.cuh) ---
@@ -118,6 +124,16 @@ __device__ __forceinline__ void tc_st16(uint32_t taddr, const float (&v)[16]) {
         : "memory");
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+// the same load without its wait (tc_ld_wait() completes it)
+__device__ __forceinline__ void tc_ld16_async(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tc_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 // generic-proxy writes to shared memory visible to the tensor cores
 __device__ __forceinline__ void tc_fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -140,14 +156,18 @@ __device__ __forceinline__ uint32_t tc_sw128(int row, int el) {
 //   softmax warps    wait s_ready: max, P, sums, rescale O; arrive p_ready;
 //   0-3              after the head: wait o_ready, write the partials,
 //                    arrive o_free; before each head: Q, arrive q_ready
+// An item: one (group, prefix partition, head group); its nh heads run one
+// after another.  Items are taken in a static order: it = blockIdx.x,
+// blockIdx.x + gridDim.x, ...
 struct TcItem {
-    int hg, part, first, n, nh;
+    int it, hg, part, first, n, nh;
     const int32_t* bt_row;
 };
 
 __device__ __forceinline__ TcItem tc_item(const PrefixParams& pp, int it) {
     const DecodeParams& a = pp.d;
     TcItem r;
+    r.it = it;
     r.hg = it % a.HG;
     const int packed = a.ws.pitems[it / a.HG];
     const int gi = packed >> 16;
@@ -178,23 +198,30 @@ prefix_tc_kernel(PrefixParams pp, const __grid_constant__ CUtensorMap tmk,
     const uint32_t bar_q = bar_empty + 8 * kTcStages;  // Q written (128 arrivals)
     const uint32_t bar_s0 = bar_q + 8;                 // S buffer 0 ready (commit)
     const uint32_t bar_s1 = bar_s0 + 8;                // S buffer 1 ready (commit)
-    const uint32_t bar_p = bar_s1 + 8;                 // P written, O rescaled (128)
-    const uint32_t bar_pv = bar_p + 8;                 // a chunk's P.V done (commit)
+    // P of chunk k written (and O rescaled), one barrier per P buffer (128
+    // arrivals): the softmax may finish P(k) and P(k + 1) before the MMA
+    // warp first looks for P(k), but never P(k + 2), which needs S(k + 2),
+    // issued only after P(k) has been taken -- so each barrier is at most
+    // one phase ahead of its waiter
+    const uint32_t bar_p0 = bar_s1 + 8;
+    const uint32_t bar_pv = bar_p0 + 8;                // a chunk's P.V done (commit)
     const uint32_t bar_o = bar_pv + 8;                 // O complete (commit)
-    const uint32_t bar_of = bar_o + 8;                 // O read out (128)
-    const uint32_t bar_end = bar_of + 8;               // final commit
+    const uint32_t bar_end = bar_o + 8;                // final commit
+    const uint32_t bar_p1 = bar_end + 8;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kTcBarOff + 16 * kTcStages + 72);
-    float* red = reinterpret_cast<float*>(smem + kTcBarOff + 256);  // [4 warps][16]
-    float* mrun = red + 64;
-    float* lrun = mrun + 16;
+    float* red = reinterpret_cast<float*>(smem + kTcBarOff + 256);  // [4 warps][16] maxima
+    float* reds = red + 64;                                           // [4 warps][16] sums
+    float* mrun = reds + 64;  // per member: the reference max of P (log2 units)
+    float* lrun = mrun + 16;  // per member: running sum of P
     float* corr = lrun + 16;
     float* mnew = corr + 16;
     // [0] abort, [1] last-partition bits, [2] tiles consumed, [4] tiles issued
     volatile int* sh = reinterpret_cast<volatile int*>(mnew + 16);
+    int* s_np = const_cast<int*>(sh) + 32;  // [16] partition counts of the unit's members
 
     const int PT = *a.ws.pt;
     const int nt = (PT + kTcTile - 1) / kTcTile;
-    const int total = *a.ws.n_pitems * a.HG;
+    const int total = *a.ws.n_pitems * a.HG;  // items
     constexpr int R = BS < 16 ? BS : 16;  // rows per TMA box (one block holds them)
 
     // zero the ring and P once: rows a tile does not load stay finite
@@ -208,10 +235,10 @@ prefix_tc_kernel(PrefixParams pp, const __grid_constant__ CUtensorMap tmk,
         tc_mbar_init(bar_q, 128);
         tc_mbar_init(bar_s0, 1);
         tc_mbar_init(bar_s1, 1);
-        tc_mbar_init(bar_p, 128);
+        tc_mbar_init(bar_p0, 128);
+        tc_mbar_init(bar_p1, 128);
         tc_mbar_init(bar_pv, 1);
         tc_mbar_init(bar_o, 1);
-        tc_mbar_init(bar_of, 128);
         tc_mbar_init(bar_end, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         sh[0] = 0;
@@ -324,7 +351,7 @@ prefix_tc_kernel(PrefixParams pp, const __grid_constant__ CUtensorMap tmk,
             // O^T += V^T P^T over chunk c; commit pv
             auto pv_chunk = [&](int c, uint32_t k) -> bool {
                 const int nc = min(kTcChunkTiles, nt - c * kTcChunkTiles);
-                const uint32_t pbuf = sb + kTcPOff;
+                const uint32_t pbuf = sb + kTcPOff + (k & 1u) * kTcPBytes;
                 for (int i = 0; i < nc; ++i, ++g) {
                     const int stage = (int)(g % kTcStages);
                     if (!tc_mbar_wait(bar_full + 8 * stage, (uint32_t)((g / kTcStages) & 1), sh)) return false;
@@ -341,24 +368,26 @@ prefix_tc_kernel(PrefixParams pp, const __grid_constant__ CUtensorMap tmk,
                 tc_commit(bar_pv);
                 return true;
             };
-            for (int it = blockIdx.x; ok && it < total; it += gridDim.x) {
-                const TcItem item = tc_item(pp, it);
-                for (int j = 0; ok && j < item.nh; ++j, ++heads) {
-                    ok = tc_mbar_wait(bar_q, heads & 1u, sh);  // this head's Q
+            // the heads of the CTA's items, in order
+            int nheads = 0;
+            for (int it = blockIdx.x; it < total; it += gridDim.x) nheads += tc_item(pp, it).nh;
+            for (int u = 0; ok && u < nheads; ++u, ++heads) {
+                ok = tc_mbar_wait(bar_q, heads & 1u, sh);  // this head's Q
+                if (ok) tc_fence_after();
+                ok = ok && s_chunk(0, chunks);
+                for (int c = 0; ok && c < nch; ++c) {
+                    // the next chunk's scores while the softmax works on this one
+                    if (c + 1 < nch) ok = s_chunk(c + 1, chunks + c + 1);
+                    ok = ok && tc_mbar_wait(((chunks + c) & 1u) ? bar_p1 : bar_p0,
+                                            ((chunks + c) >> 1) & 1u, sh);  // P written, O rescaled
                     if (ok) tc_fence_after();
-                    ok = ok && s_chunk(0, chunks);
-                    for (int c = 0; ok && c < nch; ++c) {
-                        // the next chunk's scores while the softmax works on this one
-                        if (c + 1 < nch) ok = s_chunk(c + 1, chunks + c + 1);
-                        ok = ok && tc_mbar_wait(bar_p, (chunks + c) & 1u, sh);  // P written, O rescaled
-                        if (ok) tc_fence_after();
-                        ok = ok && pv_chunk(c, chunks + c);
-                    }
-                    chunks += nch;
-                    if (!ok) break;
-                    tc_commit(bar_o);
-                    ok = tc_mbar_wait(bar_of, heads & 1u, sh);  // O read out
+                    ok = ok && pv_chunk(c, chunks + c);
                 }
+                chunks += nch;
+                if (!ok) break;
+                // the next head's first P.V waits for its first P, which
+                // the softmax hands over only after reading this O out
+                tc_commit(bar_o);
             }
             if (!ok) fail();
             tc_commit(bar_end);  // every MMA issued so far
@@ -371,7 +400,7 @@ prefix_tc_kernel(PrefixParams pp, const __grid_constant__ CUtensorMap tmk,
         const int row = 32 * warp + lane;  // a token of a tile, then a dim of O
         const uint32_t tlane = tmem + ((uint32_t)(32 * warp) << 16);
         auto csync = [] { asm volatile("bar.sync 1, 128;" ::: "memory"); };  // these 4 warps only
-        // barrier over these 4 warps that also ANDs `ok`: all continue or all stop
+        // barriers over these 4 warps that also AND / OR a flag
         auto csync_and = [](bool v) -> bool {
             uint32_t r;
             asm volatile(
@@ -384,192 +413,318 @@ prefix_tc_kernel(PrefixParams pp, const __grid_constant__ CUtensorMap tmk,
                 : "memory");
             return r != 0;
         };
+        auto csync_or = [](bool v) -> bool {
+            uint32_t r;
+            asm volatile(
+                "{.reg .pred p, q;\n\t"
+                "setp.ne.u32 p, %1, 0;\n\t"
+                "bar.red.or.pred q, 1, 128, p;\n\t"
+                "selp.u32 %0, 1, 0, q;}"
+                : "=r"(r)
+                : "r"(v ? 1u : 0u)
+                : "memory");
+            return r != 0;
+        };
+        // The 16 members' values of one token per lane are transposed in
+        // three exchange rounds (lane bits 0, 1, 2): afterwards a lane holds
+        // two members, mt and mt + 1, for the eight tokens (lane & ~7) + 0..7.
+        const int mt = ((lane & 1) << 3) | (((lane >> 1) & 1) << 2) | (((lane >> 2) & 1) << 1);
+        // a fourth round (lane bit 3) of the max reduce-scatter leaves member
+        // mt + bit 3 in lanes 0-15
+        const int mr = mt | ((lane >> 3) & 1);
+        // the number of these 128 threads whose flag is set (a barrier)
+        auto csync_count = [](bool v) -> uint32_t {
+            uint32_t r;
+            asm volatile(
+                "{.reg .pred p;\n\t"
+                "setp.ne.u32 p, %1, 0;\n\t"
+                "bar.red.popc.u32 %0, 1, 128, p;}"
+                : "=r"(r)
+                : "r"(v ? 1u : 0u)
+                : "memory");
+            return r;
+        };
+        // this thread's 32 bytes of the members' queries of head h (rows
+        // >= n zero): member row >> 3, dims (row & 7) * 16 ..
+        auto load_q = [&](const TcItem& item, int h, uint4& v0, uint4& v1) {
+            const int m = row >> 3, d0 = (row & 7) * 16;
+            v0 = v1 = make_uint4(0u, 0u, 0u, 0u);
+            if (m < item.n) {
+                const uint4* src = reinterpret_cast<const uint4*>(
+                    static_cast<const uint16_t*>(a.q) + ((int64_t)(item.first + m) * a.H + h) * kTcD + d0);
+                v0 = __ldg(src);
+                v1 = __ldg(src + 1);
+            }
+        };
+        // ... into Q, the B operand of S^T = K Q^T, then handed to the MMA warp
+        auto write_q = [&](const uint4& v0, const uint4& v1) {
+            const int m = row >> 3, d0 = (row & 7) * 16;
+            const int c = (d0 & 63) >> 3;
+            unsigned char* qb = smem + kTcQOff + (d0 >> 6) * 2048 + (m >> 3) * 1024 + (m & 7) * 128;
+            *reinterpret_cast<uint4*>(qb + ((c ^ (m & 7)) << 4)) = v0;
+            *reinterpret_cast<uint4*>(qb + (((c + 1) ^ (m & 7)) << 4)) = v1;
+            tc_fence_async_smem();
+            tc_mbar_arrive(bar_q);
+        };
         uint32_t heads = 0, chunks = 0;
         bool ok = true;
-        for (int it = blockIdx.x; ok && it < total; it += gridDim.x) {
-            const TcItem item = tc_item(pp, it);
-            for (int j = 0; ok && j < item.nh; ++j, ++heads) {
-                const int h = item.hg * kWarps + j;
-                // the members' queries (rows >= n zero) as the B operand
+        // the CTA's heads in order; the next head's Q is written as soon as
+        // the last S^T of the current one has completed
+        int it = blockIdx.x, j = 0;
+        TcItem item;
+        if (it < total) {
+            item = tc_item(pp, it);
+            uint4 v0, v1;
+            load_q(item, item.hg * kWarps, v0, v1);
+            write_q(v0, v1);
+            if (row < 16) s_np[row] = row < item.n ? a.ws.nparts[item.first + row] : 0;
+        }
+        while (ok && it < total) {
+            const int h = item.hg * kWarps + j;
+            int it2 = it, j2 = j + 1;
+            if (j2 >= item.nh) {
+                it2 += gridDim.x;
+                j2 = 0;
+            }
+            const bool more = it2 < total;
+            const TcItem item2 = (j2 == 0 && more) ? tc_item(pp, it2) : item;
+            // the next unit's queries are fetched now and written into Q
+            // once this unit's last S^T has completed
+            uint4 nq0, nq1;
+            load_q(item2, item2.hg * kWarps + j2, nq0, nq1);
+            // per member: the reference max of P (the same in every
+            // thread), and this lane's share of the running sum of P for
+            // members mt, mt + 1 (relative to the reference)
+            float mref[16], lacc[2] = {0.f, 0.f};
+#pragma unroll
+            for (int m = 0; m < 16; ++m) mref[m] = -INFINITY;
+            // whether this thread's token of tile c0 is inside the partition
+            // with its block id in range, read one tile ahead
+            auto token_ok = [&](int c0) -> bool {
+                const int rel = c0 * kTcTile + row;
+                return rel < PT && (unsigned)__ldg(item.bt_row + (item.part * PT + rel) / BS) < (unsigned)a.NB;
+            };
+            bool valid_next = nt > 0 && token_ok(0);
+            for (int c0 = 0; c0 < nt; ++c0, ++chunks) {
+                const uint32_t kb = chunks & 1u;  // this chunk's S and P buffers
+                const bool valid = valid_next;
+                if (c0 + 1 < nt) valid_next = token_ok(c0 + 1);
+                const bool got = tc_mbar_wait(kb ? bar_s1 : bar_s0, (chunks >> 1) & 1u, sh);
+                tc_fence_after();
+                // every S^T of this head has completed: Q is free
+                if (c0 == nt - 1 && got && more) write_q(nq0, nq1);
+                float sc[16];
                 {
-                    const int m = row >> 3, d0 = (row & 7) * 16;
-                    uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
-                    if (m < item.n) {
-                        const uint4* src = reinterpret_cast<const uint4*>(
-                            static_cast<const uint16_t*>(a.q) +
-                            ((int64_t)(item.first + m) * a.H + h) * kTcD + d0);
-                        v0 = __ldg(src);
-                        v1 = __ldg(src + 1);
-                    }
-                    const int c = (d0 & 63) >> 3;
-                    unsigned char* qb = smem + kTcQOff + (d0 >> 6) * 2048 + (m >> 3) * 1024 + (m & 7) * 128;
-                    *reinterpret_cast<uint4*>(qb + ((c ^ (m & 7)) << 4)) = v0;
-                    *reinterpret_cast<uint4*>(qb + (((c + 1) ^ (m & 7)) << 4)) = v1;
+                    uint32_t r[16];
+                    tc_ld16_async(tlane + kb * kTcSCols, r);
+                    tc_ld_wait();
+#pragma unroll
+                    for (int m = 0; m < 16; ++m)
+                        sc[m] = valid ? __uint_as_float(r[m]) * a.qscale : -INFINITY;
                 }
-                if (row < 16) {
-                    mrun[row] = -INFINITY;
-                    lrun[row] = 0.f;
-                }
-                tc_fence_async_smem();
-                tc_mbar_arrive(bar_q);
-                for (int c0 = 0; ok && c0 < nt; c0 += kTcChunkTiles, ++chunks) {
-                    const int nc = min(kTcChunkTiles, nt - c0);
-                    const uint32_t kb = chunks & 1u;  // this chunk's S buffer
-                    ok = csync_and(tc_mbar_wait(kb ? bar_s1 : bar_s0, (chunks >> 1) & 1u, sh));
-                    // the previous chunk's P.V: O is complete up to it, and
-                    // P's last reader is done
-                    if (ok && c0 > 0) ok = csync_and(tc_mbar_wait(bar_pv, (chunks - 1) & 1u, sh));
+                // fast path: every score within kTcLazy of its member's
+                // reference -- one barrier, no exchange of maxima
+                bool over = !got;
+#pragma unroll
+                for (int m = 0; m < 16; ++m) over = over || sc[m] > mref[m] + kTcLazy;
+                if (csync_count(over) != 0) {
+                    ok = csync_and(got);
                     if (!ok) break;
-                    tc_fence_after();
-                    // pass 1: the chunk's max per member; this thread's valid
-                    // tokens (inside the partition, block id in range)
-                    uint32_t vmask = 0;
-                    float mx[16];
+                    // the chunk's max per member: a reduce-scatter over
+                    // the lanes (15 exchanges), then over the 4 warps
+                    {
+                        float r8[8], r4[4], r2[2];
+                        const bool u1 = lane & 1, u2 = lane & 2, u4 = lane & 4, u8 = lane & 8;
 #pragma unroll
-                    for (int m = 0; m < 16; ++m) mx[m] = -INFINITY;
-                    for (int i = 0; i < nc; ++i) {
-                        const int rel = (c0 + i) * kTcTile + row;
-                        bool valid = rel < PT;
-                        if (valid)
-                            valid = (unsigned)__ldg(item.bt_row + (item.part * PT + rel) / BS) <
-                                    (unsigned)a.NB;
-                        vmask |= valid ? (1u << i) : 0u;
-                        float s[16];
-                        tc_ld16(tlane + kb * kTcSCols + 16 * i, s);
-                        if (valid) {
+                        for (int q = 0; q < 8; ++q)
+                            r8[q] = fmaxf(u1 ? sc[8 + q] : sc[q],
+                                          __shfl_xor_sync(kFull, u1 ? sc[q] : sc[8 + q], 1));
 #pragma unroll
-                            for (int m = 0; m < 16; ++m) mx[m] = fmaxf(mx[m], s[m] * a.qscale);
-                        }
-                    }
+                        for (int q = 0; q < 4; ++q)
+                            r4[q] = fmaxf(u2 ? r8[4 + q] : r8[q],
+                                          __shfl_xor_sync(kFull, u2 ? r8[q] : r8[4 + q], 2));
 #pragma unroll
-                    for (int m = 0; m < 16; ++m) {
-#pragma unroll
-                        for (int o = 16; o >= 1; o >>= 1) mx[m] = fmaxf(mx[m], __shfl_xor_sync(kFull, mx[m], o));
-                    }
-                    if (lane == 0) {
-#pragma unroll
-                        for (int m = 0; m < 16; ++m) red[warp * 16 + m] = mx[m];
+                        for (int q = 0; q < 2; ++q)
+                            r2[q] = fmaxf(u4 ? r4[2 + q] : r4[q],
+                                          __shfl_xor_sync(kFull, u4 ? r4[q] : r4[2 + q], 4));
+                        float r1 = fmaxf(u8 ? r2[1] : r2[0], __shfl_xor_sync(kFull, u8 ? r2[0] : r2[1], 8));
+                        r1 = fmaxf(r1, __shfl_xor_sync(kFull, r1, 16));
+                        if (lane < 16) red[warp * 16 + mr] = r1;
                     }
                     csync();
+                    // a member moves its reference to the chunk's max when
+                    // that passes the reference by more than kTcLazy
                     if (row < 16) {
                         const float cm = fmaxf(fmaxf(red[row], red[16 + row]), fmaxf(red[32 + row], red[48 + row]));
-                        const float mo = mrun[row];
-                        float mn = fmaxf(mo, cm);
-                        if (mn == -INFINITY) mn = 0.f;  // nothing valid yet: any base works
-                        corr[row] = exp2f(mo - mn);
-                        mnew[row] = mn;
+                        float mo = mref[0];  // mref[row], without a dynamic register index
+#pragma unroll
+                        for (int m = 1; m < 16; ++m) mo = (m == row) ? mref[m] : mo;
+                        const bool move = cm > mo + kTcLazy;
+                        mnew[row] = move ? cm : mo;
+                        corr[row] = move ? exp2f(mo - cm) : 1.f;
                     }
                     csync();
-                    // pass 2: P (16-bit) into shared memory, sums per member
-                    float mu[16], ls[16];
 #pragma unroll
-                    for (int m = 0; m < 16; ++m) {
-                        mu[m] = mnew[m];
-                        ls[m] = 0.f;
-                    }
-                    for (int i = 0; i < nc; ++i) {
-                        float s[16];
-                        tc_ld16(tlane + kb * kTcSCols + 16 * i, s);
-                        const bool valid = (vmask >> i) & 1u;
-                        unsigned char* pb = smem + kTcPOff + i * 4096 + (row >> 6) * 2048;
-#pragma unroll
-                        for (int m = 0; m < 16; ++m) {
-                            const float p = valid ? exp2f(s[m] * a.qscale - mu[m]) : 0.f;
-                            ls[m] += p;
-                            *reinterpret_cast<uint16_t*>(pb + tc_sw128(m, row & 63)) =
-                                (uint16_t)(E::from_float2(p, 0.f) & 0xffffu);
-                        }
-                    }
-#pragma unroll
-                    for (int m = 0; m < 16; ++m) {
-#pragma unroll
-                        for (int o = 16; o >= 1; o >>= 1) ls[m] += __shfl_xor_sync(kFull, ls[m], o);
-                    }
-                    if (lane == 0) {
-#pragma unroll
-                        for (int m = 0; m < 16; ++m) red[warp * 16 + m] = ls[m];
-                    }
-                    csync();
-                    if (row < 16) {
-                        lrun[row] = lrun[row] * corr[row] +
-                                    ((red[row] + red[16 + row]) + (red[32 + row] + red[48 + row]));
-                        mrun[row] = mnew[row];
-                    }
-                    // a later chunk rescales what O holds so far
+                    for (int m = 0; m < 16; ++m) mref[m] = mnew[m];
+                    lacc[0] *= corr[mt];
+                    lacc[1] *= corr[mt + 1];
+                    // what O holds so far is rescaled once the previous
+                    // chunk's P.V has landed in it
                     if (c0 > 0) {
+                        ok = csync_and(tc_mbar_wait(bar_pv, (chunks - 1) & 1u, sh));
+                        if (!ok) break;
+                        tc_fence_after();
                         float o[16];
                         tc_ld16(tlane + kTcOCol, o);
 #pragma unroll
                         for (int m = 0; m < 16; ++m) o[m] *= corr[m];
                         tc_st16(tlane + kTcOCol, o);
                     }
-                    csync();  // running sums settled before the next chunk reads red
-                    tc_fence_async_smem();
-                    tc_fence_before();
-                    tc_mbar_arrive(bar_p);
                 }
-                if (!ok) break;
-                ok = csync_and(tc_mbar_wait(bar_o, heads & 1u, sh));
-                if (!ok) break;
-                tc_fence_after();
+                // P = 2^(s - reference), 16 bits, into this chunk's P
+                // buffer (B operand, K-major, 128-byte swizzle): the
+                // values are transposed across lanes so that each lane
+                // writes two 16-byte chunks of 8 tokens (members mt,
+                // mt + 1) and sums the same values
                 {
-                    float o[16];
-                    tc_ld16(tlane + kTcOCol, o);
-                    const int d = row;
+                    float p[16];
 #pragma unroll
-                    for (int m = 0; m < 16; ++m) {
-                        if (m < item.n) {
-                            const int s = item.first + m;
-                            const int np = a.ws.nparts[s];
-                            if (np == 1) {
-                                const float l = lrun[m];
-                                const float inv = l > 0.f ? 1.f / l : 0.f;
-                                static_cast<uint16_t*>(a.out)[((int64_t)s * a.H + h) * kTcD + d] =
-                                    (uint16_t)(E::from_float2(o[m] * inv, 0.f) & 0xffffu);
-                            } else {
-                                const int64_t idx = ((int64_t)s * a.H + h) * a.max_parts + item.part;
-                                a.ws.acc[idx * kTcD + d] = o[m];
-                                if (d == 0) {
-                                    a.ws.m[idx] = mrun[m];
-                                    a.ws.l[idx] = lrun[m];
-                                }
+                    for (int m = 0; m < 16; ++m) p[m] = valid ? exp2f(sc[m] - mref[m]) : 0.f;
+                    float a8[8][2], a4[4][4], a2[2][8];
+                    const bool u1 = lane & 1, u2 = lane & 2, u4 = lane & 4;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float keep = u1 ? p[8 + q] : p[q];
+                        const float recv = __shfl_xor_sync(kFull, u1 ? p[q] : p[8 + q], 1);
+                        a8[q][0] = u1 ? recv : keep;
+                        a8[q][1] = u1 ? keep : recv;
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+#pragma unroll
+                        for (int t = 0; t < 2; ++t) {
+                            const float keep = u2 ? a8[4 + q][t] : a8[q][t];
+                            const float recv = __shfl_xor_sync(kFull, u2 ? a8[q][t] : a8[4 + q][t], 2);
+                            a4[q][t] = u2 ? recv : keep;
+                            a4[q][2 + t] = u2 ? keep : recv;
+                        }
+                    }
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            const float keep = u4 ? a4[2 + q][t] : a4[q][t];
+                            const float recv = __shfl_xor_sync(kFull, u4 ? a4[q][t] : a4[2 + q][t], 4);
+                            a2[q][t] = u4 ? recv : keep;
+                            a2[q][4 + t] = u4 ? keep : recv;
+                        }
+                    }
+                    const int tb = 32 * warp + (lane & 24);  // the first of the lane's 8 tokens
+                    unsigned char* pt = smem + kTcPOff + kb * kTcPBytes + (tb >> 6) * 2048;
+                    const int ch = (tb & 63) >> 3;           // its 16-byte chunk of a 128-byte row
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        const int m = mt + q;
+                        uint4 v;
+                        v.x = E::from_float2(a2[q][0], a2[q][1]);
+                        v.y = E::from_float2(a2[q][2], a2[q][3]);
+                        v.z = E::from_float2(a2[q][4], a2[q][5]);
+                        v.w = E::from_float2(a2[q][6], a2[q][7]);
+                        *reinterpret_cast<uint4*>(pt + (m >> 3) * 1024 + (m & 7) * 128 + ((ch ^ (m & 7)) << 4)) = v;
+                        lacc[q] += ((a2[q][0] + a2[q][1]) + (a2[q][2] + a2[q][3])) +
+                                   ((a2[q][4] + a2[q][5]) + (a2[q][6] + a2[q][7]));
+                    }
+                }
+                // each thread hands its part of P to the MMA warp
+                tc_fence_async_smem();
+                tc_fence_before();
+                tc_mbar_arrive(kb ? bar_p1 : bar_p0);
+            }
+            if (!ok) break;
+            // the head's sums per member: over the lanes that share the
+            // member (lane bits 3, 4), then over the warps
+            lacc[0] += __shfl_xor_sync(kFull, lacc[0], 8);
+            lacc[0] += __shfl_xor_sync(kFull, lacc[0], 16);
+            lacc[1] += __shfl_xor_sync(kFull, lacc[1], 8);
+            lacc[1] += __shfl_xor_sync(kFull, lacc[1], 16);
+            if (lane < 8) {
+                reds[warp * 16 + mt] = lacc[0];
+                reds[warp * 16 + mt + 1] = lacc[1];
+            }
+            ok = csync_and(tc_mbar_wait(bar_o, heads & 1u, sh));
+            if (!ok) break;
+            tc_fence_after();
+            if (row < 16) {
+                float mo = mref[0];
+#pragma unroll
+                for (int m = 1; m < 16; ++m) mo = (m == row) ? mref[m] : mo;
+                lrun[row] = (reds[row] + reds[16 + row]) + (reds[32 + row] + reds[48 + row]);
+                mrun[row] = mo;
+            }
+            csync();
+            {
+                float o[16];
+                tc_ld16(tlane + kTcOCol, o);
+                const int d = row;
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    if (m < item.n) {
+                        const int s = item.first + m;
+                        const int np = s_np[m];
+                        if (np == 1) {
+                            const float l = lrun[m];
+                            const float inv = l > 0.f ? 1.f / l : 0.f;
+                            static_cast<uint16_t*>(a.out)[((int64_t)s * a.H + h) * kTcD + d] =
+                                (uint16_t)(E::from_float2(o[m] * inv, 0.f) & 0xffffu);
+                        } else {
+                            const int64_t idx = ((int64_t)s * a.H + h) * a.max_parts + item.part;
+                            a.ws.acc[idx * kTcD + d] = o[m];
+                            if (d == 0) {
+                                a.ws.m[idx] = mrun[m];
+                                a.ws.l[idx] = lrun[m];
                             }
                         }
                     }
                 }
-                tc_fence_before();
-                tc_mbar_arrive(bar_of);
             }
             if (!ok) break;
-            // tickets of the members that have more than one partition
-            __threadfence();
-            csync();
-            if (row < 16) {
-                unsigned bit = 0;
-                if (row < item.n) {
-                    const int s = item.first + row;
-                    const int np = a.ws.nparts[s];
-                    if (np > 1) {
-                        const unsigned done = atomicAdd(&a.ws.tickets[s * a.HG + item.hg], 1u);
-                        bit = (done == (unsigned)(np - 1)) ? (1u << row) : 0u;
+            ++heads;
+            if (j2 == 0) {
+                // the item is done: tickets of the members that have more
+                // than one partition
+                __threadfence();
+                csync();
+                if (row < 16) {
+                    unsigned bit = 0;
+                    if (row < item.n) {
+                        const int s = item.first + row;
+                        const int np = s_np[row];
+                        if (np > 1) {
+                            const unsigned done = atomicAdd(&a.ws.tickets[s * a.HG + item.hg], 1u);
+                            bit = (done == (unsigned)(np - 1)) ? (1u << row) : 0u;
+                        }
+                    }
+#pragma unroll
+                    for (int o = 8; o >= 1; o >>= 1) bit |= __shfl_xor_sync(0xffffu, bit, o);
+                    if (row == 0) sh[1] = (int)bit;
+                }
+                csync();
+                unsigned last = (unsigned)sh[1];
+                if (last) {
+                    __threadfence();
+                    const int hm = item.hg * kWarps + warp;
+                    while (last) {
+                        const int m = __ffs(last) - 1;
+                        last &= last - 1;
+                        if (hm < a.H) merge_partitions<E, kTcD>(a, item.first + m, hm, s_np[m], lane);
                     }
                 }
-#pragma unroll
-                for (int o = 8; o >= 1; o >>= 1) bit |= __shfl_xor_sync(0xffffu, bit, o);
-                if (row == 0) sh[1] = (int)bit;
+                csync();  // sh[1] and s_np read by all before the next item writes them
+                if (more && row < 16) s_np[row] = row < item2.n ? a.ws.nparts[item2.first + row] : 0;
             }
-            csync();
-            unsigned last = (unsigned)sh[1];
-            if (last) {
-                __threadfence();
-                const int h = item.hg * kWarps + warp;
-                while (last) {
-                    const int m = __ffs(last) - 1;
-                    last &= last - 1;
-                    if (h < a.H) merge_partitions<E, kTcD>(a, item.first + m, h, a.ws.nparts[item.first + m], lane);
-                }
-            }
-            csync();  // sh[1] read by all before the next item writes it
+            it = it2;
+            j = j2;
+            item = item2;
         }
         if (!ok) fail();
     }
