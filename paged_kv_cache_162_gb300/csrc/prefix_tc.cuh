@@ -4,25 +4,32 @@
 //
 // Two CTAs of 6 warps per SM take the same work items as prefix_kernel --
 // (group, prefix partition, group of 4 heads) -- in a static order (the
-// items are all the same size), and for each head run
+// items are all the same size), and for each head run, per 128-token tile,
 //
 //   S^T = K Q^T    tcgen05.mma kind::f16, M = 128 tokens, N = 16 members,
-//                  K = 128 dims; A = a K tile (K-major), B = Q (K-major);
-//                  accumulator in TMEM, one 16-column slice per tile, two
-//                  buffers so the next chunk's scores overlap this softmax
-//   softmax        warps 0-3, one token per TMEM lane (tcgen05.ld); max and
-//                  sum per member across the warps; P rounded to 16 bits
-//                  into shared memory in the B layout of the next product
+//                  K = 128 dims; A = the K tile (K-major), B = Q (K-major);
+//                  accumulator in TMEM, two buffers so the next tile's
+//                  scores overlap this tile's softmax
+//   softmax        warps 0-3, one token per TMEM lane (tcgen05.ld).  Each
+//                  member keeps a reference max, moved only when a tile's
+//                  max passes it by more than kTcLazy: the common tile costs
+//                  one barrier (did any score pass its reference?) and no
+//                  exchange of maxima, and O is rescaled only when a
+//                  reference moves.  P = 2^(s - reference), rounded to 16
+//                  bits, is transposed across lanes and stored as 16-byte
+//                  chunks of the B operand of the next product (two
+//                  buffers); its sums are kept per lane until the head ends
 //   O^T += V^T P^T tcgen05.mma, M = 128 dims, N = 16 members, K = 128
-//                  tokens; A = a V tile read MN-major, B = P (K-major)
+//                  tokens; A = the V tile read MN-major, B = P (K-major)
 //
 // Warp 4 loads: K and V tiles of 128 tokens by TMA (cp.async.bulk.tensor,
 // boxes of min(bs, 16) rows x 128 bytes, 128-byte swizzle; the lanes look up
 // their blocks and issue their boxes together) into a 3-stage ring with a
 // full and an empty mbarrier per stage.  Warp 5 issues the MMAs (one
-// thread).  mbarriers hand each chunk and head between the roles.  Each
-// member's (max, sum, output) partial goes to the decode kernel's workspace
-// slots and the same tickets merge it.
+// thread).  mbarriers hand each tile and head between the roles; the next
+// head's Q is written as soon as the current head's last S^T has completed.
+// Each member's (reference, sum, output) partial goes to the decode kernel's
+// workspace slots and the same tickets merge it.
 //
 // Every wait is bounded: on a timeout the roles stop, the kernel sets
 // PKV_DEVERR_TIMEOUT, waits (bounded) for its loads in flight, frees its
@@ -149,16 +156,19 @@ __device__ __forceinline__ uint32_t tc_sw128(int row, int el) {
 // ---- the kernel -----------------------------------------------------------
 // Items are the same size, so each CTA takes items b, b + grid, b + 2*grid,
 // ... and every role walks that sequence on its own.  Per item, per head,
-// per softmax chunk of up to 8 tiles:
-//   loader warp 4    K tiles of the chunk, then its V tiles, into the ring
-//   MMA warp 5       S^T slices (K tiles), commit s_ready; wait p_ready;
-//                    O^T += V^T P^T (V tiles); after the head: commit o_ready
-//   softmax warps    wait s_ready: max, P, sums, rescale O; arrive p_ready;
-//   0-3              after the head: wait o_ready, write the partials,
-//                    arrive o_free; before each head: Q, arrive q_ready
+// per tile (a chunk is one tile):
+//   loader warp 4    the head's K tile 0, then K tile c + 1 and V tile c
+//                    for each c, into the ring
+//   MMA warp 5       wait q_ready; S^T(0); for each c: S^T(c + 1), commit
+//                    s_ready[(c + 1) & 1]; wait p_ready[c & 1]; O^T += V^T
+//                    P^T(c), commit pv; after the head: commit o_ready
+//   softmax warps    wait s_ready[c & 1]: reference check (one barrier), P,
+//   0-3              sums, arrive p_ready[c & 1]; on the head's last tile
+//                    write the next head's Q, arrive q_ready; after the
+//                    head: wait o_ready, write the partials; after the item:
+//                    tickets and merges
 // An item: one (group, prefix partition, head group); its nh heads run one
-// after another.  Items are taken in a static order: it = blockIdx.x,
-// blockIdx.x + gridDim.x, ...
+// after another.
 struct TcItem {
     int it, hg, part, first, n, nh;
     const int32_t* bt_row;
