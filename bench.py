@@ -413,6 +413,16 @@ def run_ours(args):
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         time.sleep(0.3)
+        # warm up again after the sampler's start-up pause, so that a short
+        # timed region does not begin on a GPU that has just idled for 0.3 s
+        # (measured: 20 timed steps 171.5 us per step after the pause, 168.4
+        # us with this, 168.8 us over 5000 steps)
+        with torch.cuda.stream(stream):
+            for _ in range(max(3, args.warmup)):
+                step()
+        stream.synchronize()
+        barrier()
+        torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             t_start.record(stream)
             for _ in range(K):
