@@ -2,6 +2,9 @@
 
 Each translation unit compiles in parallel; the link uses the shared CUDA
 runtime so the library and PyTorch share one runtime in a process.
+
+PKV_NVTX=1 in the environment builds the library with an NVTX range around
+every C-ABI call (for profilers); the default build has none.
 """
 from __future__ import annotations
 
@@ -45,8 +48,18 @@ def _inputs():
     return srcs + [os.path.join(INCLUDE, "pagedkv.h"), os.path.abspath(__file__)]
 
 
+FLAGS = os.path.join(BUILD, "flags.txt")
+
+
+def _defines() -> list[str]:
+    return ["-DPKV_NVTX"] if os.environ.get("PKV_NVTX", "") not in ("", "0") else []
+
+
 def up_to_date() -> bool:
     if not os.path.exists(LIB):
+        return False
+    built = open(FLAGS).read() if os.path.exists(FLAGS) else ""
+    if built != " ".join(_defines()):
         return False
     t = os.path.getmtime(LIB)
     return all(os.path.getmtime(p) <= t for p in _inputs())
@@ -60,6 +73,7 @@ def _compile(src: str, extra: list[str]) -> str:
                "-Xptxas", "-warn-spills", *inc, *extra, "-c", src, "-o", obj]
     else:
         cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", "-Wextra", *inc,
+               *[x for x in extra if x.startswith("-D")],
                "-I", os.path.join(cuda_home(), "include"), "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -73,7 +87,7 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     if not force and up_to_date():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
-    extra = ["-Xptxas", "-v"] if verbose_ptxas else []
+    extra = (["-Xptxas", "-v"] if verbose_ptxas else []) + _defines()
     srcs = [os.path.join(CSRC, s) for s in CU_SOURCES + CXX_SOURCES]
     with cf.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
         objs = list(ex.map(lambda s: _compile(s, extra), srcs))
@@ -85,6 +99,8 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(FLAGS, "w") as f:
+        f.write(" ".join(_defines()))
     return LIB
 
 

@@ -59,6 +59,7 @@ bool valid_id(const pkv_allocator* a, int32_t id) { return id >= 0 && id < a->nu
 extern "C" {
 
 pkv_status pkv_alloc_create(int32_t num_blocks, pkv_allocator** out) {
+    PKV_TRACE("pkv_alloc_create");
     pkv::clear_error();
     if (!out || num_blocks < 0) return pkv::fail(PKV_ERR_INVALID_ARG, "alloc_create: bad argument");
     pkv_allocator* a = new (std::nothrow) pkv_allocator();
@@ -81,6 +82,7 @@ pkv_status pkv_alloc_create(int32_t num_blocks, pkv_allocator** out) {
 
 pkv_status pkv_alloc_create_with_order(int32_t num_blocks, const int32_t* initial_free,
                                        int32_t n_free, pkv_allocator** out) {
+    PKV_TRACE("pkv_alloc_create_with_order");
     pkv::clear_error();
     if (!out || num_blocks < 0 || n_free < 0 || n_free > num_blocks || (n_free && !initial_free))
         return pkv::fail(PKV_ERR_INVALID_ARG, "alloc_create_with_order: bad argument");
@@ -110,6 +112,7 @@ pkv_status pkv_alloc_create_with_order(int32_t num_blocks, const int32_t* initia
 void pkv_alloc_destroy(pkv_allocator* a) { delete a; }
 
 pkv_status pkv_alloc_blocks(pkv_allocator* a, int32_t n, int32_t* out_ids) {
+    PKV_TRACE("pkv_alloc_blocks");
     pkv::clear_error();
     if (!a || n < 0 || (n && !out_ids)) return pkv::fail(PKV_ERR_INVALID_ARG, "alloc_blocks: bad argument");
     if (a->top < n) return pkv::fail(PKV_ERR_OOM, "alloc_blocks: out of free blocks");
@@ -118,6 +121,7 @@ pkv_status pkv_alloc_blocks(pkv_allocator* a, int32_t n, int32_t* out_ids) {
 }
 
 pkv_status pkv_alloc_incref(pkv_allocator* a, const int32_t* ids, int32_t n) {
+    PKV_TRACE("pkv_alloc_incref");
     pkv::clear_error();
     if (!a || n < 0 || (n && !ids)) return pkv::fail(PKV_ERR_INVALID_ARG, "alloc_incref: bad argument");
     for (int32_t i = 0; i < n; ++i)
@@ -128,6 +132,7 @@ pkv_status pkv_alloc_incref(pkv_allocator* a, const int32_t* ids, int32_t n) {
 }
 
 pkv_status pkv_alloc_decref(pkv_allocator* a, const int32_t* ids, int32_t n, int32_t* num_freed) {
+    PKV_TRACE("pkv_alloc_decref");
     pkv::clear_error();
     if (!a || n < 0 || (n && !ids)) return pkv::fail(PKV_ERR_INVALID_ARG, "alloc_decref: bad argument");
     // validate with multiplicity: a block listed k times needs rc >= k
@@ -152,6 +157,7 @@ pkv_status pkv_alloc_decref(pkv_allocator* a, const int32_t* ids, int32_t n, int
 }
 
 pkv_status pkv_alloc_cow(pkv_allocator* a, int32_t id, int32_t* out_id, int32_t* needs_copy) {
+    PKV_TRACE("pkv_alloc_cow");
     pkv::clear_error();
     if (!a || !out_id || !needs_copy || !valid_id(a, id) || a->rc[id] <= 0)
         return pkv::fail(PKV_ERR_INVALID_ARG, "alloc_cow: bad argument or block not held");
@@ -171,6 +177,7 @@ pkv_status pkv_alloc_cow(pkv_allocator* a, int32_t id, int32_t* out_id, int32_t*
 pkv_status pkv_alloc_append(pkv_allocator* a, int32_t* table, int32_t* num_blocks,
                             int32_t max_blocks, int32_t ctx_before, int32_t n_new, int32_t bs,
                             int64_t* pairs, int32_t* n_pairs) {
+    PKV_TRACE("pkv_alloc_append");
     pkv::clear_error();
     if (!a || !num_blocks || !n_pairs || bs <= 0 || ctx_before < 0 || n_new < 0 ||
         *num_blocks < 0 || *num_blocks > max_blocks || (max_blocks > 0 && !table))
@@ -215,6 +222,7 @@ pkv_status pkv_alloc_append_batch(pkv_allocator* a, int32_t* tables, int32_t* nu
                                   int32_t S, int32_t MB, const int32_t* ctx_before,
                                   const int32_t* n_new, int32_t bs, int64_t* pairs,
                                   int32_t max_pairs, int32_t* n_pairs, int32_t* n_done) {
+    PKV_TRACE("pkv_alloc_append_batch");
     pkv::clear_error();
     if (!a || S < 0 || MB < 0 || (S > 0 && (!num_blocks || !ctx_before || !n_new)) ||
         (S > 0 && MB > 0 && !tables) || !n_pairs || !n_done || max_pairs < 0 ||
@@ -257,6 +265,7 @@ pkv_status pkv_alloc_append_batch(pkv_allocator* a, int32_t* tables, int32_t* nu
 
 pkv_status pkv_alloc_fork(pkv_allocator* a, int32_t* tables, int32_t* num_blocks, int32_t S,
                           int32_t MB, const int32_t* parents) {
+    PKV_TRACE("pkv_alloc_fork");
     pkv::clear_error();
     if (!a || S < 0 || MB < 0 || (S > 0 && (!num_blocks || !parents)) || (S > 0 && MB > 0 && !tables))
         return pkv::fail(PKV_ERR_INVALID_ARG, "alloc_fork: bad argument");
@@ -333,6 +342,7 @@ pkv_status pkv_alloc_refcount(const pkv_allocator* a, int32_t id, int32_t* rc) {
 }
 
 pkv_status pkv_check_copy_pairs(const int64_t* pairs, int32_t P, int32_t NB) {
+    PKV_TRACE("pkv_check_copy_pairs");
     pkv::clear_error();
     if (P < 0 || NB < 0 || (P > 0 && !pairs)) return pkv::fail(PKV_ERR_INVALID_ARG, "check_copy_pairs: bad argument");
     char msg[160];

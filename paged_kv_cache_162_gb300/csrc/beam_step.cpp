@@ -63,6 +63,7 @@ pkv_status pkv_beam_step(pkv_allocator* a, int32_t* tables, int32_t* num_blocks,
                          int G, int H, int D, int bs, int NB,
                          float scale, pkv_dtype dtype, int partition_tokens, void* workspace,
                          size_t workspace_bytes, int32_t* n_pairs, void* stream) {
+    PKV_TRACE("pkv_beam_step");
     pkv::clear_error();
     if (!a || S <= 0 || MB <= 0 || !tables || !num_blocks || !context_lens || !parents ||
         !staging || !dev_inputs || !n_pairs || bs <= 0 || G < 0 || (G > 0 && !prefix_groups))

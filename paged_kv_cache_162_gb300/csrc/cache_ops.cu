@@ -127,6 +127,7 @@ extern "C" {
 pkv_status pkv_compute_slot_mapping(int64_t* slot_mapping, const int32_t* block_tables,
                                     const int32_t* seq_idx, const int32_t* pos, int T, int S,
                                     int MB, int bs, void* stream) {
+    PKV_TRACE("pkv_compute_slot_mapping");
     pkv::clear_error();
     if (T < 0 || S < 0 || MB < 0 || bs <= 0)
         return pkv::fail(PKV_ERR_INVALID_ARG, "compute_slot_mapping: bad size");
@@ -143,6 +144,7 @@ pkv_status pkv_compute_slot_mapping(int64_t* slot_mapping, const int32_t* block_
 pkv_status pkv_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
                                  const int64_t* slot_mapping, int T, int H, int D, int bs, int NB,
                                  pkv_dtype dtype, void* stream) {
+    PKV_TRACE("pkv_reshape_and_cache");
     pkv::clear_error();
     if (T < 0 || H <= 0 || NB < 0 || (dtype != PKV_F16 && dtype != PKV_BF16))
         return pkv::fail(PKV_ERR_INVALID_ARG, "reshape_and_cache: bad size or dtype");
@@ -164,6 +166,7 @@ pkv_status pkv_reshape_and_cache(const void* key, const void* value, void* k_cac
 
 pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_mapping, int P,
                            int H, int D, int bs, int NB, pkv_dtype dtype, void* stream) {
+    PKV_TRACE("pkv_copy_blocks");
     pkv::clear_error();
     if (P < 0 || H <= 0 || NB < 0 || (dtype != PKV_F16 && dtype != PKV_BF16))
         return pkv::fail(PKV_ERR_INVALID_ARG, "copy_blocks: bad size or dtype");
@@ -186,6 +189,7 @@ pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_ma
 pkv_status pkv_swap_blocks(void* gpu_k, void* gpu_v, void* host_k, void* host_v,
                            const int64_t* block_mapping, int P, int H, int D, int bs, int NB_gpu,
                            int NB_host, pkv_dtype dtype, int direction, void* stream) {
+    PKV_TRACE("pkv_swap_blocks");
     pkv::clear_error();
     if (P < 0 || H <= 0 || NB_gpu < 0 || NB_host < 0 || (dtype != PKV_F16 && dtype != PKV_BF16) ||
         (direction != PKV_SWAP_OUT && direction != PKV_SWAP_IN))

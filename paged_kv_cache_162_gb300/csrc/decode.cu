@@ -1524,6 +1524,7 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_ca
                                       int NB, int MB, int max_context_len, float scale,
                                       pkv_dtype dtype, int partition_tokens, void* workspace,
                                       size_t workspace_bytes, void* stream) {
+    PKV_TRACE("pkv_paged_attention_decode");
     static const char* who = "paged_attention_decode";
     pkv::clear_error();
     if (S > 0 && workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
@@ -1549,6 +1550,7 @@ pkv_status pkv_decode_step(void* out, const void* q, const void* key, const void
                            int S, int H, int D, int bs, int NB, int MB, int max_context_len,
                            float scale, pkv_dtype dtype, int partition_tokens, void* workspace,
                            size_t workspace_bytes, void* stream) {
+    PKV_TRACE("pkv_decode_step");
     static const char* who = "decode_step";
     pkv::clear_error();
     if (T < 0 || T == INT32_MAX) return pkv::fail(PKV_ERR_INVALID_ARG, "decode_step: bad token count");
@@ -1610,6 +1612,7 @@ pkv_status pkv_paged_attention_decode_shared_prefix(
     const int32_t* block_tables, const int32_t* context_lens, const int32_t* prefix_groups, int G,
     int S, int H, int D, int bs, int NB, int MB, int max_context_len, float scale, pkv_dtype dtype,
     int partition_tokens, void* workspace, size_t workspace_bytes, void* stream) {
+    PKV_TRACE("pkv_paged_attention_decode_shared_prefix");
     static const char* who = "paged_attention_decode_shared_prefix";
     pkv::clear_error();
     if (G < 0 || G > 32767 || (G > 0 && !prefix_groups))
@@ -1710,6 +1713,7 @@ extern "C" pkv_status pkv_paged_attention_decode_noalloc(
     const int32_t* block_tables, const int32_t* context_lens, int S, int H, int D, int bs, int NB,
     int MB, int max_context_len, float scale, pkv_dtype dtype, int partition_tokens,
     void* stream) {
+    PKV_TRACE("pkv_paged_attention_decode_noalloc");
     static const char* who = "paged_attention_decode_noalloc";
     pkv::clear_error();
     CallShape cs;

@@ -106,6 +106,7 @@ const char* pkv_last_error_string(void) { return t_last_error.c_str(); }
 const char* pkv_version(void) { return "pagedkv 0.1 (sm_103a)"; }
 
 pkv_status pkv_sync_check(void* stream) {
+    PKV_TRACE("pkv_sync_check");
     pkv::clear_error();
     cudaError_t e = cudaStreamSynchronize(pkv::as_stream(stream));
     if (e != cudaSuccess) return pkv::cuda_fail(e, "sync_check");
@@ -115,6 +116,7 @@ pkv_status pkv_sync_check(void* stream) {
 }
 
 pkv_status pkv_get_device_errors(int32_t* flags) {
+    PKV_TRACE("pkv_get_device_errors");
     pkv::clear_error();
     if (!flags) return pkv::fail(PKV_ERR_INVALID_ARG, "get_device_errors: null");
     int* w = pkv::device_error_word();
@@ -131,6 +133,7 @@ pkv_status pkv_get_device_errors(int32_t* flags) {
 }
 
 pkv_status pkv_selftest_bounded_wait(int64_t polls, void* stream) {
+    PKV_TRACE("pkv_selftest_bounded_wait");
     pkv::clear_error();
     if (polls < 1 || polls > kTcWaitLimit)
         return pkv::fail(PKV_ERR_INVALID_ARG, "selftest_bounded_wait: polls must be in [1, 2^20]");

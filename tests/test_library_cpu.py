@@ -459,3 +459,21 @@ def test_check_copy_pairs_accepts_allocator_copies_and_names_the_bad_pair():
             check_copy_pairs(np.array(p, np.int64), 40)
         assert e.value.status == L.PKV_ERR_INVALID_ARG and what in str(e.value), (what, e.value)
     assert L.lib().pkv_check_copy_pairs(None, -1, 40) == L.PKV_ERR_INVALID_ARG
+
+
+def test_nvtx_ranges_only_in_the_traced_build(tmp_path):
+    """PKV_NVTX builds an NVTX range into every C-ABI call; the default
+    build carries none (the host sources are compiled both ways)."""
+    import shutil
+    import subprocess
+    from paged_kv_cache_162_gb300 import _build
+    if shutil.which("g++") is None or shutil.which("nm") is None:
+        pytest.skip("needs g++ and nm")
+    inc = ["-I", _build.INCLUDE, "-I", _build.CSRC, "-I", os.path.join(_build.cuda_home(), "include")]
+    for src in ("allocator.cpp", "beam_step.cpp"):
+        for flag, want in ((["-DPKV_NVTX"], True), ([], False)):
+            obj = str(tmp_path / (src + ("_nvtx" if flag else "") + ".o"))
+            subprocess.run(["g++", "-O2", "-std=c++17", "-fPIC", *inc, *flag, "-c",
+                            os.path.join(_build.CSRC, src), "-o", obj], check=True)
+            syms = subprocess.run(["nm", obj], check=True, capture_output=True, text=True).stdout
+            assert ("nvtx" in syms.lower()) == want, (src, flag)
