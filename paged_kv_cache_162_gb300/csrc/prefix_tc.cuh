@@ -170,14 +170,13 @@ __device__ __forceinline__ uint32_t tc_sw128(int row, int el) {
 // An item: one (group, prefix partition, head group); its nh heads run one
 // after another.
 struct TcItem {
-    int it, hg, part, first, n, nh;
+    int hg, part, first, n, nh;
     const int32_t* bt_row;
 };
 
 __device__ __forceinline__ TcItem tc_item(const PrefixParams& pp, int it) {
     const DecodeParams& a = pp.d;
     TcItem r;
-    r.it = it;
     r.hg = it % a.HG;
     const int packed = a.ws.pitems[it / a.HG];
     const int gi = packed >> 16;
