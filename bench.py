@@ -416,10 +416,18 @@ def run_ours(args):
         # warm up again after the sampler's start-up pause, so that a short
         # timed region does not begin on a GPU that has just idled for 0.3 s
         # (measured: 20 timed steps 171.5 us per step after the pause, 168.4
-        # us with this, 168.8 us over 5000 steps)
+        # us with this, 168.8 us over 5000 steps).  It runs for at least
+        # 0.25 s, so the sampler (one sample per 100 ms) also records the
+        # clocks under this load right before a timed region that may be
+        # only a few milliseconds long.
+        t_warm = time.perf_counter()
+        n_warm = 0
         with torch.cuda.stream(stream):
-            for _ in range(max(3, args.warmup)):
+            while n_warm < max(3, args.warmup) or time.perf_counter() - t_warm < 0.25:
                 step()
+                n_warm += 1
+                if n_warm % 32 == 0:
+                    stream.synchronize()  # keep the host within 32 steps of the GPU
         stream.synchronize()
         barrier()
         torch.cuda.synchronize()
