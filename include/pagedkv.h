@@ -477,6 +477,46 @@ pkv_status pkv_beam_step(
     int H, int D, int bs, int NB, float scale, pkv_dtype dtype, int partition_tokens,
     void* workspace, size_t workspace_bytes, int32_t* n_pairs, void* stream);
 
+/* ------------------------------------------------------------------ *
+ * A beam search held on the native side: pkv_beam_step with everything
+ * that stays the same from step to step given once, and the alternation
+ * of two staging buffers done here ([P1] 3.3.2 share_blocks; [P4]
+ * "Memory Sharing与写时复制": the beams of a search fork and diverge
+ * step after step over one pool).
+ *
+ * pkv_beam_search_create keeps the pointers and sizes (all of them as
+ * pkv_beam_step takes them; the caller still owns every buffer and keeps it
+ * alive until pkv_beam_search_destroy) and creates one CUDA event per
+ * staging buffer on the current device.  staging0 and staging1: pinned
+ * host memory, 256-byte aligned, inputs_bytes each.
+ * Errors: PKV_ERR_INVALID_ARG (null pointer, bad size, misaligned buffer,
+ * inputs_bytes < pkv_beam_inputs_bytes(S, MB)) before any CUDA call;
+ * PKV_ERR_CUDA if an event cannot be created; PKV_ERR_HOST_MEMORY. */
+typedef struct pkv_beam_search pkv_beam_search;
+
+pkv_status pkv_beam_search_create(
+    pkv_allocator* a, int32_t* tables, int32_t* num_blocks, int32_t* context_lens, int32_t S,
+    int32_t MB, void* staging0, void* staging1, void* dev_inputs, size_t inputs_bytes, void* out,
+    void* k_cache, void* v_cache, int64_t* slot_mapping, const int32_t* prefix_groups, int G,
+    int H, int D, int bs, int NB, float scale, pkv_dtype dtype, int partition_tokens,
+    void* workspace, size_t workspace_bytes, pkv_beam_search** out_search);
+
+/* One step of the search: waits (on the host) until the upload from the
+ * staging buffer used two steps ago has finished, runs pkv_beam_step with
+ * that buffer, records the buffer's event on `stream` (whatever the
+ * outcome), and returns the step's copy pairs: *n_pairs of them at
+ * *pairs ([n][2] int64, (src, dst)), inside that staging buffer and valid
+ * until the step after next.  parents [S] host int32; q, key, value
+ * [S][H][D] device.  Errors are pkv_beam_step's; PKV_ERR_CUDA if the wait
+ * or the event record fails. */
+pkv_status pkv_beam_search_step(pkv_beam_search* search, const int32_t* parents, const void* q,
+                                const void* key, const void* value, void* stream,
+                                int32_t* n_pairs, const int64_t** pairs);
+
+/* Destroys the events and the handle (waits for neither; the caller
+ * synchronises its stream first). */
+void pkv_beam_search_destroy(pkv_beam_search* search);
+
 #ifdef __cplusplus
 }
 #endif

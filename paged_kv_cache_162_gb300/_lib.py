@@ -94,6 +94,10 @@ SIGNATURES = {
     "pkv_beam_inputs_bytes": (_SZ, [_I32, _I32]),
     "pkv_beam_step": (_I, [_P, _P, _P, _P, _P, _I32, _I32, _P, _P, _SZ, _P, _P, _P, _P, _P, _P,
                            _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P, _P]),
+    "pkv_beam_search_create": (_I, [_P, _P, _P, _P, _I32, _I32, _P, _P, _P, _SZ, _P, _P, _P, _P,
+                                    _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P]),
+    "pkv_beam_search_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _P]),
+    "pkv_beam_search_destroy": (None, [_P]),
 }
 
 _lib = None
@@ -258,6 +262,50 @@ def pkv_beam_step(alloc_handle, tables, num_blocks, context_lens, parents, S, MB
         float(scale), int(dtype), partition_tokens, ptr(workspace), workspace_bytes,
         ctypes.addressof(n), stream_handle(stream)), "beam_step")
     return int(n.value)
+
+
+class BeamSearch:
+    """pkv_beam_search_create / _step / _destroy: a beam search whose fixed
+    arguments live on the native side, so a step is one short call.  The
+    caller keeps every buffer passed here alive as long as this object."""
+
+    def __init__(self, alloc_handle, tables, num_blocks, context_lens, S, MB, staging0, staging1,
+                 dev_inputs, inputs_bytes, out, k_cache, v_cache, slot_mapping, prefix_groups, G,
+                 H, D, bs, NB, scale, dtype, partition_tokens, workspace, workspace_bytes):
+        h = ctypes.c_void_p()
+        check(lib().pkv_beam_search_create(
+            alloc_handle, ptr(tables), ptr(num_blocks), ptr(context_lens), S, MB, ptr(staging0),
+            ptr(staging1), ptr(dev_inputs), int(inputs_bytes), ptr(out), ptr(k_cache),
+            ptr(v_cache), ptr(slot_mapping), ptr(prefix_groups), G, H, D, bs, NB, float(scale),
+            int(dtype), partition_tokens, ptr(workspace), int(workspace_bytes),
+            ctypes.addressof(h)), "beam_search_create")
+        self._h = h
+        self._n = ctypes.c_int32(0)
+        self._pairs = ctypes.c_void_p()  # receives the int64 pairs pointer
+        self._n_addr = ctypes.addressof(self._n)
+        self._pairs_addr = ctypes.addressof(self._pairs)
+        self._step = lib().pkv_beam_search_step
+
+    def step(self, parents_addr: int, q_addr: int, key_addr: int, value_addr: int,
+             stream: int):
+        """One step (addresses as ints, stream as a handle); returns (number
+        of copy pairs, address of the first pair)."""
+        st = self._step(self._h, parents_addr, q_addr, key_addr, value_addr, stream, self._n_addr,
+                        self._pairs_addr)
+        if st != PKV_OK:
+            check(st, "beam_search_step")
+        return self._n.value, self._pairs.value
+
+    def close(self) -> None:
+        if self._h:
+            lib().pkv_beam_search_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def pkv_selftest_bounded_wait(polls: int, stream=None) -> None:

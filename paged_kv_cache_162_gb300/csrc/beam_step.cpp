@@ -17,6 +17,7 @@
 
 #include <cstdint>
 #include <cstring>
+#include <new>
 
 #include "pagedkv.h"
 #include "pkv_internal.h"
@@ -136,6 +137,111 @@ pkv_status pkv_beam_step(pkv_allocator* a, int32_t* tables, int32_t* num_blocks,
                            prefix_groups, G, S, S, H, D, bs, NB, MB, 0, scale, dtype,
                            partition_tokens, workspace,
                            workspace_bytes, stream);
+}
+
+struct pkv_beam_search {
+    pkv_allocator* a;
+    int32_t *tables, *num_blocks, *context_lens;
+    int32_t S, MB;
+    void* staging[2];
+    void* dev_inputs;
+    size_t inputs_bytes;
+    void *out, *k_cache, *v_cache;
+    int64_t* slot_mapping;
+    const int32_t* prefix_groups;
+    int G, H, D, bs, NB;
+    float scale;
+    pkv_dtype dtype;
+    int partition_tokens;
+    void* workspace;
+    size_t workspace_bytes;
+    size_t pairs_offset;
+    cudaEvent_t done[2];
+    bool used[2];
+    int turn;
+};
+
+pkv_status pkv_beam_search_create(
+    pkv_allocator* a, int32_t* tables, int32_t* num_blocks, int32_t* context_lens, int32_t S,
+    int32_t MB, void* staging0, void* staging1, void* dev_inputs, size_t inputs_bytes, void* out,
+    void* k_cache, void* v_cache, int64_t* slot_mapping, const int32_t* prefix_groups, int G,
+    int H, int D, int bs, int NB, float scale, pkv_dtype dtype, int partition_tokens,
+    void* workspace, size_t workspace_bytes, pkv_beam_search** out_search) {
+    PKV_TRACE("pkv_beam_search_create");
+    pkv::clear_error();
+    if (!out_search) return pkv::fail(PKV_ERR_INVALID_ARG, "beam_search_create: null handle pointer");
+    *out_search = nullptr;
+    if (!a || S <= 0 || MB <= 0 || !tables || !num_blocks || !context_lens || !staging0 ||
+        !staging1 || !dev_inputs || !out || !k_cache || !v_cache || !slot_mapping || !workspace ||
+        bs <= 0 || G < 0 || (G > 0 && !prefix_groups))
+        return pkv::fail(PKV_ERR_INVALID_ARG, "beam_search_create: bad argument");
+    const BeamLayout L = beam_layout(S, MB);
+    if (inputs_bytes < L.total)
+        return pkv::fail(PKV_ERR_INVALID_ARG, "beam_search_create: staging/device input buffers too small");
+    for (const void* p : {staging0, staging1, dev_inputs})
+        if (reinterpret_cast<uintptr_t>(p) & 255u)
+            return pkv::fail(PKV_ERR_INVALID_ARG, "beam_search_create: input buffers must be 256-byte aligned");
+    pkv_beam_search* b = new (std::nothrow) pkv_beam_search();
+    if (!b) return pkv::fail(PKV_ERR_HOST_MEMORY, "beam_search_create: out of host memory");
+    *b = pkv_beam_search{a, tables, num_blocks, context_lens, S, MB, {staging0, staging1},
+                         dev_inputs, inputs_bytes, out, k_cache, v_cache, slot_mapping,
+                         prefix_groups, G, H, D, bs, NB, scale, dtype, partition_tokens,
+                         workspace, workspace_bytes, L.pairs, {nullptr, nullptr}, {false, false}, 0};
+    for (int i = 0; i < 2; ++i) {
+        const cudaError_t e = cudaEventCreateWithFlags(&b->done[i], cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            if (i == 1) cudaEventDestroy(b->done[0]);
+            delete b;
+            return pkv::fail(PKV_ERR_CUDA, "beam_search_create: cudaEventCreate failed");
+        }
+    }
+    *out_search = b;
+    return PKV_OK;
+}
+
+pkv_status pkv_beam_search_step(pkv_beam_search* b, const int32_t* parents, const void* q,
+                                const void* key, const void* value, void* stream,
+                                int32_t* n_pairs, const int64_t** pairs) {
+    PKV_TRACE("pkv_beam_search_step");
+    pkv::clear_error();
+    if (!b || !parents || !n_pairs || !pairs)
+        return pkv::fail(PKV_ERR_INVALID_ARG, "beam_search_step: bad argument");
+    const int slot = b->turn;
+    b->turn ^= 1;
+    if (b->used[slot]) {
+        // the upload from this buffer two steps ago must be done before
+        // the buffer is written again
+        const cudaError_t e = cudaEventSynchronize(b->done[slot]);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return pkv::fail(PKV_ERR_CUDA, "beam_search_step: waiting for the staging buffer failed");
+        }
+    }
+    const pkv_status st = pkv_beam_step(
+        b->a, b->tables, b->num_blocks, b->context_lens, parents, b->S, b->MB, b->staging[slot],
+        b->dev_inputs, b->inputs_bytes, b->out, q, key, value, b->k_cache, b->v_cache,
+        b->slot_mapping, b->prefix_groups, b->G, b->H, b->D, b->bs, b->NB, b->scale, b->dtype,
+        b->partition_tokens, b->workspace, b->workspace_bytes, n_pairs, stream);
+    // recorded whatever the outcome: a failure after the upload was queued
+    // still leaves it in flight
+    const cudaError_t e = cudaEventRecord(b->done[slot], reinterpret_cast<cudaStream_t>(stream));
+    b->used[slot] = true;
+    *pairs = reinterpret_cast<const int64_t*>(static_cast<unsigned char*>(b->staging[slot]) +
+                                              b->pairs_offset);
+    if (st != PKV_OK) return st;
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return pkv::fail(PKV_ERR_CUDA, "beam_search_step: event record failed");
+    }
+    return PKV_OK;
+}
+
+void pkv_beam_search_destroy(pkv_beam_search* b) {
+    if (!b) return;
+    for (int i = 0; i < 2; ++i)
+        if (b->done[i]) cudaEventDestroy(b->done[i]);
+    delete b;
 }
 
 }  // extern "C"

@@ -218,8 +218,11 @@ class DecodeStep:
     def plan(self):
         """Host allocator: tables and copy-on-write pairs for this step.
         A new plan also starts a new beam search (beam_step)."""
-        for name in ("beam_ctx", "_beam_args"):
-            self.__dict__.pop(name, None)
+        for name in ("beam_ctx", "_beam_native"):
+            old = self.__dict__.pop(name, None)
+            if name == "_beam_native" and old is not None:
+                torch.cuda.synchronize(self.device)  # its staging buffers may still be in flight
+                old.close()
         self.allocator = BlockAllocator(self.NB, self.initial_free)
         ids, counts = np.unique(self.tables_pre[self.tables_pre >= 0], return_counts=True)
         for b, c in zip(ids.tolist(), counts.tolist()):
@@ -313,13 +316,21 @@ class DecodeStep:
         o_pos = o_ctx + up(4 * S)
         o_seq = o_pos + up(4 * S)
         self._beam_offsets = {"ctx": o_ctx, "pos": o_pos, "seq": o_seq, "pairs": o_seq + up(4 * S)}
-        self._beam_npairs = ctypes.c_int32(0)
         # the step's device inputs, as views of the uploaded buffer
         d = self._beam_dev_inputs
         self._beam_views = (d[:4 * S * MB].view(torch.int32).view(S, MB),
                             d[o_ctx:o_ctx + 4 * S].view(torch.int32),
                             d[o_pos:o_pos + 4 * S].view(torch.int32),
                             d[o_seq:o_seq + 4 * S].view(torch.int32))
+        self._beam_stg_base = [sl["stg"].data_ptr() for sl in self._beam_slots]
+        # the native side of the search: every argument of pkv_beam_step
+        # that stays the same, and the alternation of the staging buffers
+        self._beam_native = L.BeamSearch(
+            self.allocator._h, self.tables_host, self.nblocks_host, self.beam_ctx, S, MB,
+            self._beam_slots[0]["stg"], self._beam_slots[1]["stg"], self._beam_dev_inputs, nb,
+            self.out, self.k_cache, self.v_cache, self.slot_mapping, self._beam_groups_dev,
+            self._beam_G, self.H, self.D, self.bs, self.NB, self.scale, dtype_code(self.dtype),
+            self.partition_tokens, self._beam_ws, self._beam_ws.numel())
 
     def beam_step(self, parents, new_k, new_v, q, stream=None):
         """One beam-search step after plan(): every sequence b continues from
@@ -336,56 +347,43 @@ class DecodeStep:
             self.nblocks_host = np.ascontiguousarray(self.nblocks_host, dtype=np.int32)
             self.tables_host = np.ascontiguousarray(self.tables_host, dtype=np.int32)
             self._beam_buffers()
-        st = stream if stream is not None else torch.cuda.current_stream()
-        slot = self._beam_slots[self._beam_turn]
-        self._beam_turn ^= 1
-        if slot["used"]:
-            slot["done"].synchronize()
+        sh = stream.cuda_stream if stream is not None else torch.cuda.current_stream().cuda_stream
         n = S * H * D
-        on_device = all(isinstance(t, torch.Tensor) and t.is_cuda for t in (q, new_k, new_v))
-        if on_device:
+        if (isinstance(q, torch.Tensor) and isinstance(new_k, torch.Tensor)
+                and isinstance(new_v, torch.Tensor) and q.is_cuda and new_k.is_cuda and new_v.is_cuda):
             for t in (q, new_k, new_v):
                 if t.element_size() != 2 or t.numel() != n or not t.is_contiguous():
                     raise L.PkvError(L.PKV_ERR_INVALID_ARG,
                                      "beam_step: q/new_k/new_v must be contiguous [S, H, D] 16-bit")
             tq, tk, tv = q, new_k, new_v
         else:
+            # host arrays: through a pinned buffer (two used in turn, each
+            # guarded by an event) into the device token buffer
+            slot = self._beam_slots[self._beam_turn]
+            self._beam_turn ^= 1
+            if slot["used"]:
+                slot["done"].synchronize()
             u16 = slot["u16"].numpy().view(np.uint16)
             u16[:n] = np.asarray(q).ravel()
             u16[n:2 * n] = np.asarray(new_k).ravel()
             u16[2 * n:] = np.asarray(new_v).ravel()
+            st = stream if stream is not None else torch.cuda.current_stream()
             with torch.cuda.stream(st):
                 self._beam_dev_u16.copy_(slot["u16"], non_blocking=True)
+            slot["done"].record(st)
+            slot["used"] = True
             tok = self._beam_dev_u16.view(self.dtype)
             tq, tk, tv = (tok[:n].view(S, H, D), tok[n:2 * n].view(S, H, D),
                           tok[2 * n:].view(S, H, D))
         par = np.ascontiguousarray(parents, dtype=np.int32)
-        if getattr(self, "_beam_args", None) is None:
-            # the pointers that stay the same from step to step
-            self._beam_args = (
-                self.allocator._h, self.tables_host.ctypes.data, self.nblocks_host.ctypes.data,
-                self.beam_ctx.ctypes.data, self._beam_dev_inputs.data_ptr(),
-                self._beam_inputs_bytes, self.out.data_ptr(), self.k_cache.data_ptr(),
-                self.v_cache.data_ptr(), self.slot_mapping.data_ptr(),
-                None if self._beam_groups_dev is None else self._beam_groups_dev.data_ptr(),
-                self._beam_G, self._beam_ws.data_ptr(), self._beam_ws.numel(),
-                ctypes.addressof(self._beam_npairs))
-        (h, p_tab, p_nb, p_ctx, p_dev, nbytes, p_out, p_k, p_v, p_slot, p_grp, G, p_ws, ws_n,
-         p_n) = self._beam_args
         t0 = time.perf_counter()
-        status = L.lib().pkv_beam_step(
-            h, p_tab, p_nb, p_ctx, par.ctypes.data, S, MB, slot["stg"].data_ptr(), p_dev, nbytes,
-            p_out, tq.data_ptr(), tk.data_ptr(), tv.data_ptr(), p_k, p_v, p_slot, p_grp, G, H, D,
-            bs, self.NB, self.scale, dtype_code(self.dtype), self.partition_tokens, p_ws, ws_n,
-            p_n, st.cuda_stream)
+        P, at = self._beam_native.step(par.ctypes.data, tq.data_ptr(), tk.data_ptr(), tv.data_ptr(),
+                                       sh)
         self.last_native_seconds = time.perf_counter() - t0
-        L.check(status, "beam_step")
-        P = self._beam_npairs.value
-        slot["done"].record(st)
-        slot["used"] = True
-        o = self._beam_offsets["pairs"]
-        pairs = (slot["stg_np"][o:o + 16 * P].view(np.int64).reshape(P, 2).copy() if P
-                 else np.empty((0, 2), dtype=np.int64))
+        # the pairs sit in the staging buffer the step used
+        k = 0 if 0 <= at - self._beam_stg_base[0] < self._beam_inputs_bytes else 1
+        o = at - self._beam_stg_base[k]
+        pairs = self._beam_slots[k]["stg_np"][o:o + 16 * P].view(np.int64).reshape(P, 2).copy()
         self.pairs_host = pairs
         self.context_lens_host = self.beam_ctx
         self.T = S

@@ -477,3 +477,34 @@ def test_nvtx_ranges_only_in_the_traced_build(tmp_path):
                             os.path.join(_build.CSRC, src), "-o", obj], check=True)
             syms = subprocess.run(["nm", obj], check=True, capture_output=True, text=True).stdout
             assert ("nvtx" in syms.lower()) == want, (src, flag)
+
+
+def test_beam_search_create_rejects_bad_arguments_before_any_cuda_call():
+    """The beam-search handle checks its arguments on the host first: a
+    null handle pointer, a missing allocator, buffers that are too small or
+    misaligned are refused (no GPU is needed to see it)."""
+    lib = L.lib()
+    h = ctypes.c_void_p()
+    a = BlockAllocator(64)
+    S, MB = 4, 8
+    tables = np.zeros((S, MB), np.int32)
+    nb = np.zeros(S, np.int32)
+    ctx = np.zeros(S, np.int32)
+    need = L.pkv_beam_inputs_bytes(S, MB)
+    raw = np.zeros(4 * need + 1024, np.uint8)
+    base = raw.ctypes.data + (-raw.ctypes.data) % 256
+    stg0, stg1, dev = base, base + need + (-need % 256), base + 2 * (need + (-need % 256))
+    fake = base  # any non-null address: nothing is dereferenced before the checks fail
+
+    def create(alloc_h, s0, inputs_bytes, out_ptr):
+        return lib.pkv_beam_search_create(alloc_h, tables.ctypes.data, nb.ctypes.data,
+                                          ctx.ctypes.data, S, MB, s0, stg1, dev, inputs_bytes,
+                                          fake, fake, fake, fake, None, 0, 4, 64, 16, 64, 0.125,
+                                          L.PKV_F16, 0, fake, 1 << 20, out_ptr)
+    assert create(a._h, stg0, need, None) == L.PKV_ERR_INVALID_ARG
+    assert create(None, stg0, need, ctypes.addressof(h)) == L.PKV_ERR_INVALID_ARG
+    assert create(a._h, stg0, need - 1, ctypes.addressof(h)) == L.PKV_ERR_INVALID_ARG
+    assert create(a._h, stg0 + 16, need, ctypes.addressof(h)) == L.PKV_ERR_INVALID_ARG
+    assert "aligned" in L.pkv_last_error_string()
+    assert h.value is None
+    lib.pkv_beam_search_destroy(None)  # a null handle is a no-op
