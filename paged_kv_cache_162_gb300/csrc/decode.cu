@@ -50,7 +50,10 @@
 //  * Shared prefixes: when sequences share the blocks of a prefix, a
 //    prefix kernel (mma.sync, or tcgen05 + TMA in prefix_tc.cuh) reads each
 //    shared block once for all members of the group; the decode kernel then
-//    covers only the members' own tokens, and the tickets merge both.
+//    covers only the members' own tokens.  The prefix kernel has completed
+//    when the decode kernel begins, so a member whose own tokens are one
+//    partition merges the prefix partials into it in registers; otherwise
+//    the tickets merge both.
 //  * Safety: a table entry outside [0, NB) or a context outside
 //    [0, max_context_len] is never dereferenced; the kernel masks it and
 //    sets a bit in the device error word.  No CTA ever waits on another.
@@ -304,8 +307,10 @@ __device__ __forceinline__ void plan_cta(const PlanArgs& pa) {
     // shared prefixes: every member of group g skips the first pp_g
     // partitions, which the prefix kernel computes for all members at once
     __shared__ int s_full_skip, s_pitems;
-    if (G > 0) {
+    if (ws.pre_parts) {  // read by the decode kernel whenever present
         for (int s = tid; s < S; s += kPlanThreads) ws.pre_parts[s] = 0;
+    }
+    if (G > 0) {
         if (tid == 0) { s_full_skip = 0; s_pitems = 0; }
         __syncthreads();
         for (int g = tid; g < G; g += kPlanThreads) {
@@ -545,10 +550,13 @@ constexpr int kWarpWindow = 64;  // table entries one warp holds in shared memor
 
 // `wtab` is this warp's window of kWarpWindow table entries in shared
 // memory, refilled (by the whole warp) when a tile's block falls outside it.
+// `pre`: the leading partitions of the sequence that a prefix kernel has
+// already written (it completed before this kernel began).  When this is the
+// sequence's one other partition, the output is merged here (fused).
 template <class E, int D, int BS>
 __device__ __forceinline__ void attend_partition(const DecodeParams& a, int s, int h, int part,
-                                                 int t_begin, int t_end, int np, int lane,
-                                                 int* wtab) {
+                                                 int t_begin, int t_end, int np, int pre,
+                                                 int lane, int* wtab) {
     constexpr int LPR = D / 8;         // lanes per row: 16 bytes each
     constexpr int RPI = 32 / LPR;      // rows per warp-wide load
     constexpr int NI = kTile / RPI;    // warp-wide loads per tile (K and V each)
@@ -699,6 +707,33 @@ __device__ __forceinline__ void attend_partition(const DecodeParams& a, int s, i
             *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + ((int64_t)s * a.H + h) * D +
                                       c * 8) = pkv::pack8<E>(acc);
         }
+    } else if (pre > 0 && np - pre == 1) {
+        // the prefix partials 0 .. pre-1 are complete: fold each into this
+        // partition's (max, sum, output), one load round per partial, and
+        // write the normalised output -- no partial, no ticket
+        if (lane < LPR) {
+            const int64_t base = ((int64_t)s * a.H + h) * a.max_parts;
+            float M = m_run, L = l_run;
+            for (int p = 0; p < pre; ++p) {
+                const float mp = __ldcg(a.ws.m + base + p);
+                const float lp = __ldcg(a.ws.l + base + p);
+                const float4* src = reinterpret_cast<const float4*>(a.ws.acc + (base + p) * D + c * 8);
+                const float4 x0 = __ldcg(src), x1 = __ldcg(src + 1);
+                const float Mn = fmaxf(M, mp);
+                const float wo = (M == -INFINITY) ? 0.f : exp2f(M - Mn);
+                const float wp = (mp == -INFINITY) ? 0.f : exp2f(mp - Mn);
+                const float xp[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[j] = fmaf(wp, xp[j], acc[j] * wo);
+                L = fmaf(wp, lp, L * wo);
+                M = Mn;
+            }
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] *= inv;
+            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + ((int64_t)s * a.H + h) * D +
+                                      c * 8) = pkv::pack8<E>(acc);
+        }
     } else {
         const int64_t idx = ((int64_t)s * a.H + h) * a.max_parts + part;
         if (lane < LPR) {
@@ -819,12 +854,15 @@ __global__ void __launch_bounds__(kThreads, PKV_MIN_CTAS_PER_SM) decode_kernel(D
         const int packed = a.ws.items[item / a.HG];
         const int s = packed >> 16, part = packed & 0xffff;
         const int np = a.ws.nparts[s];
+        // partitions a prefix kernel wrote before this kernel began
+        const int pre = a.ws.pre_parts ? a.ws.pre_parts[s] : 0;
         const int ctx = clamp_ctx(a.context_lens[s], a.max_ctx);
         const int t_begin = part * PT;
         const int t_end = min(t_begin + PT, ctx);
         const int h = hg * kWarps + warp;
-        if (h < a.H) attend_partition<E, D, BS>(a, s, h, part, t_begin, t_end, np, lane, s_tab[warp]);
-        if (np > 1) {
+        if (h < a.H)
+            attend_partition<E, D, BS>(a, s, h, part, t_begin, t_end, np, pre, lane, s_tab[warp]);
+        if (np > 1 && !(pre > 0 && np - pre == 1)) {
             __threadfence();
             __syncthreads();
             if (threadIdx.x == 0) {
