@@ -336,12 +336,33 @@ __device__ __forceinline__ void plan_cta(const PlanArgs& pa) {
         __syncthreads();
     }
 
-    // item order: how full are the partial partitions?
+    // Item order.  Partial partitions go first when they are full enough,
+    // else last.  With prefix groups the items left are the members' own
+    // tokens; when some of them are long (a partial of PT / 8 tokens or
+    // more), full partitions go first and then the partial ones longest
+    // first (64 length classes), so that no long item starts last.  The
+    // class counts and positions are taken with one shared-memory atomic per
+    // class present in a warp: same-address atomics from every lane would
+    // serialise when the lengths fall in a class or two.
+    __shared__ int s_longest_first;
+    auto len_class = [&](int rem) { return 63 - (int)min(63LL, (long long)rem * 64 / PT); };
+    __shared__ int s_cls[64];                // per class: count, then next position
     __shared__ long long s_fill[kWarpsP];
     __shared__ int s_partials_first;
+    if (tid < 64) s_cls[tid] = 0;
+    __syncthreads();
     {
         long long fill = 0;
-        for (int s = tid; s < S; s += kPlanThreads) fill += clamp_ctx(context_lens[s], max_ctx) % PT;
+        for (int base = 0; base < S; base += kPlanThreads) {  // the same trip count in every lane
+            const int s = base + tid;
+            const int c = s < S ? clamp_ctx(context_lens[s], max_ctx) : PT;
+            if (s < S) fill += c % PT;
+            if (G > 0) {  // one atomic per class present in the warp
+                const int cls = (s < S && (c % PT != 0 || c == 0)) ? len_class(c % PT) : 64;
+                const unsigned same = __match_any_sync(kFull, cls);
+                if (cls != 64 && (same & ((1u << lane) - 1u)) == 0u) atomicAdd(&s_cls[cls], __popc(same));
+            }
+        }
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) fill += __shfl_xor_sync(kFull, fill, o);
         if (lane == 0) s_fill[wid] = fill;
@@ -352,10 +373,27 @@ __device__ __forceinline__ void plan_cta(const PlanArgs& pa) {
             for (int w = 0; w < kWarpsP; ++w) f += s_fill[w];
             s_partials_first = 8 * f >= 3 * (long long)(s_items - s_full_total) * PT;
         }
+        if (G > 0 && wid == 0) {  // class counts -> first positions
+            const int c0 = s_cls[2 * lane], c1 = s_cls[2 * lane + 1];
+            // classes 0 .. 55: partials of PT / 8 tokens or more
+            const unsigned long_ones = __ballot_sync(kFull, (2 * lane <= 55 && c0 > 0) ||
+                                                               (2 * lane + 1 <= 55 && c1 > 0));
+            if (lane == 0) s_longest_first = long_ones != 0u;
+            int incl = c0 + c1;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int x = __shfl_up_sync(kFull, incl, o);
+                if (lane >= o) incl += x;
+            }
+            const int excl = incl - c0 - c1;
+            s_cls[2 * lane] = excl;
+            s_cls[2 * lane + 1] = excl + c0;
+        }
         __syncthreads();
     }
     const int n_partial = s_items - s_full_total;
-    const bool partials_first = s_partials_first != 0;
+    const bool longest_first = G > 0 && s_longest_first != 0;
+    const bool partials_first = s_partials_first != 0 && !longest_first;
     for (int base = 0; base < S; base += kPlanThreads) {
         const int s = base + tid;
         int nf = 0, np = 0, skip = 0;
@@ -364,6 +402,17 @@ __device__ __forceinline__ void plan_cta(const PlanArgs& pa) {
             nf = c / PT;
             np = (c % PT != 0 || c == 0) ? 1 : 0;  // an empty context still writes zeros
             skip = G > 0 ? ws.pre_parts[s] : 0;
+        }
+        // longest first: this sequence's partial item goes to its class's
+        // next position (one atomic per class present in the warp)
+        int my_pos = 0;
+        if (longest_first) {
+            const int cls = np ? len_class(clamp_ctx(context_lens[s], max_ctx) % PT) : 64;
+            const unsigned same = __match_any_sync(kFull, cls);
+            const int rank = __popc(same & ((1u << lane) - 1u));
+            int first = 0;
+            if (cls != 64 && rank == 0) first = atomicAdd(&s_cls[cls], __popc(same));
+            my_pos = __shfl_sync(kFull, first, __ffs(same) - 1) + rank;
         }
         int a = nf - skip, b = np;
 #pragma unroll
@@ -377,7 +426,8 @@ __device__ __forceinline__ void plan_cta(const PlanArgs& pa) {
         for (int w = 0; w < wid; ++w) { off_f += wsum[0][w]; off_p += wsum[1][w]; }
         if (s < S) {
             const int at_f = partials_first ? n_partial + off_f : off_f;
-            const int at_p = partials_first ? off_p : s_full_total + off_p;
+            const int at_p = longest_first ? s_full_total + my_pos
+                                           : partials_first ? off_p : s_full_total + off_p;
             for (int k = skip; k < nf; ++k) ws.items[at_f + k - skip] = (s << 16) | k;
             if (np) ws.items[at_p] = (s << 16) | nf;
             ws.nparts[s] = nf + np;
