@@ -70,6 +70,21 @@ def test_shared_prefix_full_workload(cow):
     assert_attention_close(out_to_double(st.out), r["ref"].out, "shared prefix full")
 
 
+def test_many_members_with_long_tails():
+    """384 members (48 prompts x 8 samples), so the plan places the partial
+    items in two chunks of its threads, with tails up to 256 tokens, so the
+    longest-first order is on; each member's tail is one partition and is
+    merged with the prefix partial in registers."""
+    w = W.shared_prefix(seed=23, prompts=48, samples=8, prefix=1024, tail_lo=1, tail_hi=256, H=8,
+                        D=128)
+    r = compare_step(w)
+    st = r["step"]
+    st.out.fill_(float("nan"))
+    st.decode_shared_prefix(_groups(w, 8, 1024))
+    torch.cuda.synchronize()
+    assert_attention_close(out_to_double(st.out), r["ref"].out, "384 members, long tails")
+
+
 @pytest.mark.parametrize("scale", [0.0, -0.2])
 def test_zero_and_negative_scale(scale):
     """The softmax max must be taken after scaling: with a negative scale the
