@@ -508,3 +508,13 @@ def test_beam_search_create_rejects_bad_arguments_before_any_cuda_call():
     assert "aligned" in L.pkv_last_error_string()
     assert h.value is None
     lib.pkv_beam_search_destroy(None)  # a null handle is a no-op
+    # a step without a handle, parents or result pointers is refused before
+    # it touches a stream or a staging buffer
+    n = ctypes.c_int32(-7)
+    pairs = ctypes.c_void_p()
+    parents = np.zeros(S, np.int32)
+    step = lib.pkv_beam_search_step
+    assert step(None, parents.ctypes.data, fake, fake, fake, None, ctypes.addressof(n),
+                ctypes.addressof(pairs)) == L.PKV_ERR_INVALID_ARG
+    assert "beam_search_step" in L.pkv_last_error_string()
+    assert n.value == -7 and pairs.value is None
